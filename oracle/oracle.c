@@ -1,0 +1,476 @@
+/*
+ * oracle.c -- plain, slow, obviously-correct CPU reference for speculative tree verification.
+ *
+ * TEST INFRASTRUCTURE ONLY: only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline leg load
+ * this library.  It shares nothing with the CUDA path.
+ *
+ * What it follows (page titles and sections of the method's public descriptions):
+ *  - "Aurora" blog post, section 2 (core idea): the target verifies the draft's proposals in parallel;
+ *    a tree-attention mask built from the speculative tree's causal structure lets every accepted and
+ *    rejected branch be processed in one batched pass; the draft is trained with an acceptance loss
+ *    (cross-entropy on accepted tokens) and a rejection loss on rejected branches.
+ *  - "TIDE" (moreh.io) overview and evaluation: drafts are verified in one target pass; the acceptance
+ *    length is the number of draft tokens the target accepts per verification step.
+ *  The pages give no formulas.  The attention is the plain masked-softmax definition; the stochastic
+ *  rule is standard speculative sampling (accept with min(1, p/q), resample from norm(max(0, p - q)));
+ *  the rejection term is -log(1 - q(token)).  The integer contract that makes acceptance reproducible
+ *  bit for bit is stated next to each function.
+ *
+ * Floating point: every accumulation is float64.  The acceptance contract is fp32 + integers by
+ * definition (see or_fx_weight) and must be compiled with -ffp-contract=off.
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+typedef unsigned __int128 u128;
+
+enum { OK = 0, E_ARG = 1, E_TREE = 2, E_BIG = 3, E_UNSUP = 4, E_NONFINITE = 5 };
+enum { DT_F32 = 0, DT_BF16 = 1, DT_E4M3 = 2 };
+
+int or_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ---------------------------------------------------------------------------------------------- */
+/* element decoding                                                                                 */
+/* ---------------------------------------------------------------------------------------------- */
+static float bf16_to_float(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* OCP 8-bit floating point E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa bits; no infinities;
+ * S.1111.111 is NaN; largest finite magnitude 448. */
+static double e4m3_to_double(uint8_t c) {
+    int e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);            /* subnormal: m/8 * 2^(1-7) */
+    else        v = ldexp((double)(8 + m), e - 10);  /* (1 + m/8) * 2^(e-7) */
+    return (c & 0x80) ? -v : v;
+}
+
+static double load_elem(const void* base, size_t i, int dt) {
+    switch (dt) {
+    case DT_F32:  return (double)((const float*)base)[i];
+    case DT_BF16: return (double)bf16_to_float(((const uint16_t*)base)[i]);
+    default:      return e4m3_to_double(((const uint8_t*)base)[i]);
+    }
+}
+
+/* float32 view of a logit (f32 or bf16 only) */
+static float load_logit(const void* base, size_t i, int dt) {
+    return dt == DT_F32 ? ((const float*)base)[i] : bf16_to_float(((const uint16_t*)base)[i]);
+}
+
+/* ---------------------------------------------------------------------------------------------- */
+/* tree                                                                                             */
+/* ---------------------------------------------------------------------------------------------- */
+/* A draft tree is a parent array: node 0 is the root (the last committed token, parent -1); every other
+ * node names an earlier node as its parent, so parent[i] < i and the array is topologically ordered. */
+int or_tree_check(int T, const int32_t* parent) {
+    if (T < 1) return E_ARG;
+    if (parent[0] != -1) return E_TREE;
+    for (int i = 1; i < T; ++i)
+        if (parent[i] < 0 || parent[i] >= i) return E_TREE;
+    return OK;
+}
+
+int or_tree_depth(int T, const int32_t* parent, int32_t* depth) {
+    int st = or_tree_check(T, parent);
+    if (st) return st;
+    for (int i = 0; i < T; ++i) {
+        int d = 0;
+        for (int a = i; parent[a] >= 0; a = parent[a]) ++d;   /* explicit walk to the root */
+        depth[i] = d;
+    }
+    return OK;
+}
+
+/* ---------------------------------------------------------------------------------------------- */
+/* tree-masked attention (plain definition, float64)                                               */
+/* ---------------------------------------------------------------------------------------------- */
+static void attn_row(int T, int Hq, int Hkv, int D, int kv_cap, int q_dt, int kv_dt, const void* q,
+                     const void* k, const void* v, const float* k_scale, const float* v_scale, int L,
+                     const int32_t* par, double scale, int b, int i, int h, double* o, double* lse_out) {
+    int G = Hq / Hkv, hk = h / G;                       /* contiguous GQA groups */
+    int on[64];
+    memset(on, 0, sizeof on);
+    for (int a = i; a >= 0; a = par[a]) on[a] = 1;       /* ancestors of i, itself and the root included */
+    double ks = (kv_dt == DT_E4M3) ? (double)k_scale[hk] : 1.0;
+    double vs = (kv_dt == DT_E4M3) ? (double)v_scale[hk] : 1.0;
+    size_t qoff = (((size_t)b * T + i) * Hq + h) * D;
+    size_t kvbase = ((size_t)b * Hkv + hk) * (size_t)kv_cap * D;
+    int npos = L + T;
+    double* s = (double*)malloc(sizeof(double) * (size_t)npos);
+    double m = -INFINITY;
+    for (int j = 0; j < npos; ++j) {
+        int allowed = j < L || on[j - L];
+        if (!allowed) { s[j] = -INFINITY; continue; }
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d)
+            acc += load_elem(q, qoff + d, q_dt) * (load_elem(k, kvbase + (size_t)j * D + d, kv_dt) * ks);
+        s[j] = scale * acc;
+        if (s[j] > m) m = s[j];
+    }
+    double sum = 0.0;
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    for (int j = 0; j < npos; ++j) {
+        if (s[j] == -INFINITY) continue;
+        double w = exp(s[j] - m);
+        sum += w;
+        for (int d = 0; d < D; ++d) o[d] += w * (load_elem(v, kvbase + (size_t)j * D + d, kv_dt) * vs);
+    }
+    for (int d = 0; d < D; ++d) o[d] /= sum;
+    *lse_out = m + log(sum);
+    free(s);
+}
+
+int or_tree_attn(int B, int T, int Hq, int Hkv, int D, int kv_cap, int q_dt, int kv_dt,
+                 const void* q, const void* k, const void* v, const float* k_scale, const float* v_scale,
+                 const int32_t* kv_len, const int32_t* parent, double sm_scale,
+                 const int32_t* rows, int n_rows, double* out, double* lse, int32_t* status) {
+    if (B < 0 || T < 1 || Hq < 1 || Hkv < 1 || D < 1 || kv_cap < 0) return E_ARG;
+    if (T > 64) return E_BIG;
+    if (Hq % Hkv) return E_ARG;
+    if (q_dt == DT_E4M3 || q_dt < 0 || q_dt > 2 || kv_dt < 0 || kv_dt > 2) return E_UNSUP;
+    if (kv_dt == DT_E4M3 && (!k_scale || !v_scale)) return E_ARG;
+    double scale = sm_scale != 0.0 ? sm_scale : 1.0 / sqrt((double)D);
+    for (int b = 0; b < B; ++b) {
+        int st = or_tree_check(T, parent + (size_t)b * T);
+        if (!st && (kv_len[b] < 0 || kv_len[b] + T > kv_cap)) st = E_ARG;
+        status[b] = st;
+    }
+    long total = rows ? n_rows : (long)B * T * Hq;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (long r = 0; r < total; ++r) {
+        int b, i, h;
+        if (rows) { b = rows[3 * r]; i = rows[3 * r + 1]; h = rows[3 * r + 2]; }
+        else { h = (int)(r % Hq); i = (int)((r / Hq) % T); b = (int)(r / ((long)Hq * T)); }
+        if (status[b]) continue;
+        size_t idx = ((size_t)b * T + i) * Hq + h;
+        attn_row(T, Hq, Hkv, D, kv_cap, q_dt, kv_dt, q, k, v, k_scale, v_scale, kv_len[b],
+                 parent + (size_t)b * T, scale, b, i, h, out + idx * D, lse + idx);
+    }
+    return OK;
+}
+
+/* ---------------------------------------------------------------------------------------------- */
+/* acceptance: the integer contract                                                                 */
+/* ---------------------------------------------------------------------------------------------- */
+/* Contract (both the oracle and the device implement it from this text):
+ *   y_k = fp32(z_k) * invT with invT = (float)(1/(double)temperature);  m = max_k y_k
+ *   d = y_k - m;  t = d * log2(e)  (fp32, each op rounded to nearest even)
+ *   t < -24  ->  W_k = 0
+ *   else n = rint(t), f = t - n,  P(f) = Horner over c7..c0 with fmaf, c_j = fp32((ln 2)^j / j!)
+ *        W_k = floor(P(f) * 2^(24 + n))           (so W at the row maximum is exactly 2^24)
+ *   S = sum_k W_k (64-bit).  p(k) is read as W_k / S. */
+static const float C_LOG2E = 0x1.715476p+0f;
+static const float C_P0 = 1.0f;
+static const float C_P1 = 0x1.62e430p-1f;
+static const float C_P2 = 0x1.ebfbe0p-3f;
+static const float C_P3 = 0x1.c6b08ep-5f;
+static const float C_P4 = 0x1.3b2ab6p-7f;
+static const float C_P5 = 0x1.5d87fep-10f;
+static const float C_P6 = 0x1.430912p-13f;
+static const float C_P7 = 0x1.ffcbfcp-17f;
+
+float or_fx_exp2(float f) {
+    float p = C_P7;
+    p = fmaf(p, f, C_P6);
+    p = fmaf(p, f, C_P5);
+    p = fmaf(p, f, C_P4);
+    p = fmaf(p, f, C_P3);
+    p = fmaf(p, f, C_P2);
+    p = fmaf(p, f, C_P1);
+    p = fmaf(p, f, C_P0);
+    return p;
+}
+
+uint32_t or_fx_weight(float y, float m) {
+    float d = y - m;
+    float t = d * C_LOG2E;
+    if (!(t >= -24.0f)) return 0u;
+    float n = rintf(t);
+    float f = t - n;
+    float w = ldexpf(or_fx_exp2(f), 24 + (int)n);
+    return (uint32_t)floorf(w);
+}
+
+void or_fx_exp2_batch(const float* f, float* out, long n) {
+    for (long i = 0; i < n; ++i) out[i] = or_fx_exp2(f[i]);
+}
+
+void or_fx_weight_batch(const float* y, float m, uint32_t* out, long n) {
+    for (long i = 0; i < n; ++i) out[i] = or_fx_weight(y[i], m);
+}
+
+typedef struct {
+    float m;       /* max of y over the row */
+    uint64_t S;    /* sum of W */
+    int finite;    /* all y finite */
+} row_stats;
+
+static row_stats row_fx_stats(const void* logits, size_t row, int V, int dt, float invT) {
+    row_stats r;
+    r.m = -INFINITY; r.S = 0; r.finite = 1;
+    size_t base = row * (size_t)V;
+    for (int k = 0; k < V; ++k) {
+        float y = load_logit(logits, base + k, dt) * invT;
+        if (!isfinite(y)) r.finite = 0;
+        if (y > r.m) r.m = y;
+    }
+    if (!r.finite) return r;
+    for (int k = 0; k < V; ++k) r.S += or_fx_weight(load_logit(logits, base + k, dt) * invT, r.m);
+    return r;
+}
+
+static void row_fx_weights(const void* logits, size_t row, int V, int dt, float invT, float m, uint64_t* w) {
+    size_t base = row * (size_t)V;
+    for (int k = 0; k < V; ++k) w[k] = or_fx_weight(load_logit(logits, base + k, dt) * invT, m);
+}
+
+/* first index of the maximum; -1 if the row holds a non-finite value */
+static int row_argmax(const void* logits, size_t row, int V, int dt) {
+    size_t base = row * (size_t)V;
+    int best = -1;
+    float bv = -INFINITY;
+    for (int k = 0; k < V; ++k) {
+        float z = load_logit(logits, base + k, dt);
+        if (!isfinite(z)) return -1;
+        if (best < 0 || z > bv) { bv = z; best = k; }
+    }
+    return best;
+}
+
+/* smallest j whose inclusive prefix sum of w exceeds floor(u * R / 2^32), R = sum of w > 0 */
+static int sample_index(const uint64_t* w, int V, uint64_t R, uint32_t u) {
+    u128 thr = ((u128)u * R) >> 32;
+    u128 run = 0;
+    for (int j = 0; j < V; ++j) {
+        run += w[j];
+        if (run > thr) return j;
+    }
+    return V - 1; /* unreachable when R = sum(w) */
+}
+
+int or_accept(int B, int T, int V, int logit_dt, const void* target, const void* draft,
+              const int32_t* tokens, const int32_t* parent, float temperature, const uint32_t* uniforms,
+              int32_t* accept_len, int32_t* path, int32_t* out_tokens, int32_t* bonus, int32_t* argmax,
+              int32_t* status) {
+    if (B < 0 || T < 1 || V < 1) return E_ARG;
+    if (T > 64) return E_BIG;
+    if (logit_dt != DT_F32 && logit_dt != DT_BF16) return E_UNSUP;
+    if (!(temperature >= 0.0f) || isinf(temperature)) return E_ARG;
+    int greedy = temperature == 0.0f;
+    if (!greedy && !uniforms) return E_ARG;
+    float invT = greedy ? 1.0f : (float)(1.0 / (double)temperature);
+
+    /* argmax of every target row, independent of the walk */
+    if (argmax) {
+#pragma omp parallel for schedule(dynamic, 8)
+        for (long r = 0; r < (long)B * T; ++r) argmax[r] = row_argmax(target, (size_t)r, V, logit_dt);
+    }
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        const int32_t* par = parent + (size_t)b * T;
+        const int32_t* tok = tokens + (size_t)b * T;
+        int32_t* pth = path + (size_t)b * T;
+        int32_t* otk = out_tokens + (size_t)b * T;
+        for (int j = 0; j < T; ++j) { pth[j] = -1; otk[j] = -1; }
+        accept_len[b] = -1;
+        bonus[b] = -1;
+        int st = or_tree_check(T, par);
+        for (int c = 1; !st && c < T; ++c)
+            if (tok[c] < 0 || tok[c] >= V) st = E_ARG;
+        if (!st) {   /* every row of the request is scanned on the device, so all must be finite */
+            for (int r = 0; r < T && !st; ++r) {
+                size_t row = (size_t)b * T + r;
+                if (greedy) {
+                    if (row_argmax(target, row, V, logit_dt) < 0) st = E_NONFINITE;
+                } else {
+                    if (!row_fx_stats(target, row, V, logit_dt, invT).finite) st = E_NONFINITE;
+                    if (draft && !row_fx_stats(draft, row, V, logit_dt, invT).finite) st = E_NONFINITE;
+                }
+            }
+        }
+        if (status) status[b] = st;
+        if (st) continue;
+
+        int n = 0, cur = 0;
+        if (greedy) {
+            /* greedy: descend to the first child (ascending node id) whose token is the target argmax */
+            for (;;) {
+                int am = row_argmax(target, (size_t)b * T + cur, V, logit_dt);
+                int next = -1;
+                for (int c = cur + 1; c < T; ++c)
+                    if (par[c] == cur && tok[c] == am) { next = c; break; }
+                if (next < 0) { bonus[b] = am; break; }
+                pth[n++] = next;
+                cur = next;
+            }
+        } else {
+            uint64_t* wres = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)V);
+            uint64_t* wq = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)V);
+            for (;;) {
+                size_t row = (size_t)b * T + cur;
+                row_stats ps = row_fx_stats(target, row, V, logit_dt, invT);
+                int has_child = 0;
+                for (int c = cur + 1; c < T; ++c) if (par[c] == cur) { has_child = 1; break; }
+                row_fx_weights(target, row, V, logit_dt, invT, ps.m, wres);
+                uint64_t Sres = ps.S;
+                if (!has_child) {
+                    bonus[b] = sample_index(wres, V, Sres, uniforms[(size_t)b * T]);
+                    break;
+                }
+                uint64_t Sq = 1;
+                if (draft) {
+                    row_stats qs = row_fx_stats(draft, row, V, logit_dt, invT);
+                    row_fx_weights(draft, row, V, logit_dt, invT, qs.m, wq);
+                    Sq = qs.S;
+                }
+                int next = -1;
+                for (int c = cur + 1; c < T; ++c) {
+                    if (par[c] != cur) continue;
+                    int x = tok[c];
+                    uint64_t wqx = draft ? wq[x] : 1u;   /* one-hot proposal: q = delta_x, Sq = 1 */
+                    u128 lhs = (u128)uniforms[(size_t)b * T + c] * wqx * Sres;
+                    u128 rhs = ((u128)wres[x] * Sq) << 32;
+                    if (lhs < rhs) { next = c; break; }
+                    /* rejected: p' <- floor(max(0, p'*Sq - q*S') / Sq), taken per token */
+                    uint64_t S2 = 0;
+                    for (int kk = 0; kk < V; ++kk) {
+                        uint64_t qk = draft ? wq[kk] : (uint64_t)(kk == x);
+                        u128 a = (u128)wres[kk] * Sq, s = (u128)qk * Sres;
+                        wres[kk] = a > s ? (uint64_t)((a - s) / Sq) : 0u;
+                        S2 += wres[kk];
+                    }
+                    Sres = S2;
+                }
+                if (next >= 0) { pth[n++] = next; cur = next; continue; }
+                if (Sres == 0) {   /* residual vanished: fall back to the target row itself */
+                    row_fx_weights(target, row, V, logit_dt, invT, ps.m, wres);
+                    Sres = ps.S;
+                }
+                bonus[b] = sample_index(wres, V, Sres, uniforms[(size_t)b * T]);
+                break;
+            }
+            free(wres);
+            free(wq);
+        }
+        accept_len[b] = n;
+        for (int j = 0; j < n; ++j) otk[j] = tok[pth[j]];
+        otk[n] = bonus[b];
+    }
+    return OK;
+}
+
+/* ---------------------------------------------------------------------------------------------- */
+/* training loss                                                                                    */
+/* ---------------------------------------------------------------------------------------------- */
+/* log(1 - e^{-a}) for a > 0, in the two-branch form that keeps full relative accuracy
+ * (log(-expm1(-a)) up to ln 2, log1p(-e^{-a}) beyond). */
+static double log1mexp(double a) {
+    return a <= M_LN2 ? log(-expm1(-a)) : log1p(-exp(-a));
+}
+
+static int loss_core(int N, int T, int V, const void* logits, int is_bf16, const int32_t* tokens,
+                     const int32_t* parent, const int32_t* labels, double* row_loss, double* row_acc,
+                     double* row_rej, double* sums, double* grad, int32_t* status) {
+    if (N < 0 || T < 1 || V < 2) return E_ARG;
+    if (T > 64) return E_BIG;
+    double n_terms = (double)N * (double)(T - 1);
+    double inv_n = n_terms > 0 ? 1.0 / n_terms : 0.0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int n = 0; n < N; ++n) {
+        const int32_t* par = parent + (size_t)n * T;
+        const int32_t* tok = tokens + (size_t)n * T;
+        const int32_t* lab = labels + (size_t)n * T;
+        int st = or_tree_check(T, par);
+        for (int c = 1; !st && c < T; ++c)
+            if (tok[c] < 0 || tok[c] >= V || lab[par[c]] < 0 || lab[par[c]] >= V) st = E_ARG;
+        double* z = (double*)malloc(sizeof(double) * (size_t)V);
+        for (int p = 0; p < T; ++p) {
+            size_t row = (size_t)n * T + p;
+            row_loss[row] = row_acc[row] = row_rej[row] = 0.0;
+            int nch = 0;
+            for (int c = p + 1; c < T && !st; ++c) if (par[c] == p) ++nch;
+            if (st || nch == 0) {
+                if (grad) memset(grad + row * V, 0, sizeof(double) * (size_t)V);
+                continue;
+            }
+            for (int k = 0; k < V; ++k)
+                z[k] = is_bf16 ? (double)bf16_to_float(((const uint16_t*)logits)[row * V + k])
+                               : ((const double*)logits)[row * V + k];
+            double m = -INFINITY;
+            for (int k = 0; k < V; ++k) if (z[k] > m) m = z[k];
+            double s = 0.0;
+            for (int k = 0; k < V; ++k) s += exp(z[k] - m);
+            double lse = m + log(s);
+            double A = 0.0, C = 0.0, acc = 0.0, rej = 0.0;
+            for (int c = p + 1; c < T; ++c) {
+                if (par[c] != p) continue;
+                int x = tok[c];
+                if (x == lab[p]) {          /* accepted: cross-entropy -log q(x) */
+                    A += 1.0;
+                    acc += lse - z[x];
+                } else {                    /* rejected: -log(1 - q(x)), q clamped to <= 1 - 1e-6 */
+                    double a = lse - z[x];
+                    if (a < 1e-6) a = 1e-6;
+                    rej += -log1mexp(a);
+                    C += 1.0 / expm1(a);    /* q/(1-q) */
+                }
+            }
+            row_acc[row] = acc;
+            row_rej[row] = rej;
+            row_loss[row] = acc + rej;
+            if (grad) {
+                double* g = grad + row * V;
+                for (int k = 0; k < V; ++k) g[k] = exp(z[k] - lse) * (A - C);
+                g[lab[p]] -= A;
+                for (int c = p + 1; c < T; ++c) {
+                    if (par[c] != p || tok[c] == lab[p]) continue;
+                    double a = lse - z[tok[c]];
+                    if (a < 1e-6) a = 1e-6;
+                    g[tok[c]] += 1.0 / expm1(a);
+                }
+                for (int k = 0; k < V; ++k) g[k] *= inv_n;
+            }
+        }
+        free(z);
+        if (status) status[n] = st;
+    }
+    double sa = 0.0, sr = 0.0;
+    for (long r = 0; r < (long)N * T; ++r) { sa += row_acc[r]; sr += row_rej[r]; }
+    sums[0] = sa;
+    sums[1] = sr;
+    sums[2] = n_terms;
+    return OK;
+}
+
+int or_loss_f64(int N, int T, int V, const double* logits, const int32_t* tokens, const int32_t* parent,
+                const int32_t* labels, double* row_loss, double* row_acc, double* row_rej, double* sums,
+                double* grad, int32_t* status) {
+    return loss_core(N, T, V, logits, 0, tokens, parent, labels, row_loss, row_acc, row_rej, sums, grad,
+                     status);
+}
+
+int or_loss(int N, int T, int V, const uint16_t* logits_bf16, const int32_t* tokens, const int32_t* parent,
+            const int32_t* labels, double* row_loss, double* row_acc, double* row_rej, double* sums,
+            double* grad, int32_t* status) {
+    return loss_core(N, T, V, logits_bf16, 1, tokens, parent, labels, row_loss, row_acc, row_rej, sums,
+                     grad, status);
+}

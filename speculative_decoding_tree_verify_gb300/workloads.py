@@ -1,0 +1,360 @@
+"""Seeded synthetic inputs for speculative tree verification.
+
+This module only *draws* inputs: draft trees (parent arrays), draft tokens, KV caches, logits, labels and
+the raw 32-bit uniforms of the acceptance test.  It holds none of the verification arithmetic (no
+attention, no acceptance rule, no loss), so it can feed both the CPU oracle and the CUDA library with
+the same bytes.
+
+Every tensor comes from its own child stream of ``numpy.random.SeedSequence(seed)`` driving a Philox
+bit generator, spawned in a fixed order, so a (workload, seed) pair always produces the same bytes.
+
+Encodings handed to both sides:
+  * ``f32``  : float32 array
+  * ``bf16`` : uint16 array holding bfloat16 bit patterns (rounded to nearest even from float32)
+  * ``e4m3`` : uint8 array holding OCP FP8 E4M3 codes (round to nearest even, saturating at 448), with a
+               float32 scale per KV head: real value = decoded code * scale[h].
+
+Tree shape (the pages give node count, depth and branching only; this is the reading used everywhere):
+level sizes n_d = min(n_{d-1} * k_d, rem - (depth - d)) with rem starting at T - 1; level d takes n_d
+distinct (parent, rank) slots drawn uniformly from the n_{d-1} * k_d candidates; nodes are numbered
+breadth-first by (parent, rank), so parent[i] < i and node 0 is the root (the last committed token).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+DTYPES = ("f32", "bf16", "e4m3")
+
+
+# ----------------------------------------------------------------------------------------------------
+# streams and encodings
+# ----------------------------------------------------------------------------------------------------
+def rng_streams(seed: int, k: int) -> list[np.random.Generator]:
+    """k independent Philox streams spawned from one seed, in a fixed order."""
+    return [np.random.Generator(np.random.Philox(s)) for s in np.random.SeedSequence(seed).spawn(k)]
+
+
+def f32_to_bf16(x) -> np.ndarray:
+    """float32 -> bfloat16 bit patterns, round to nearest even (inputs are finite)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def bf16_to_f32(h) -> np.ndarray:
+    """bfloat16 bit patterns -> float32 (exact)."""
+    return (np.ascontiguousarray(h, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def _e4m3_positive_table() -> np.ndarray:
+    # codes 0..126 (0x7F is NaN); value = (8+m) * 2^(e-10) for e >= 1, m * 2^-9 for e == 0
+    vals = np.empty(127, np.float64)
+    for c in range(127):
+        e, m = c >> 3, c & 7
+        vals[c] = m * 2.0 ** -9 if e == 0 else (8 + m) * 2.0 ** (e - 10)
+    return vals
+
+
+_E4M3_POS = _e4m3_positive_table()
+
+
+def f32_to_e4m3(x) -> np.ndarray:
+    """float -> E4M3 codes, round to nearest even, saturating to +-448."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    hi = np.clip(np.searchsorted(_E4M3_POS, a, side="left"), 1, 126)
+    lo = hi - 1
+    d_lo = a - _E4M3_POS[lo]
+    d_hi = _E4M3_POS[hi] - a
+    pick_lo = (d_lo < d_hi) | ((d_lo == d_hi) & (lo % 2 == 0))
+    code = np.where(pick_lo, lo, hi)
+    code = np.where(a >= _E4M3_POS[126], 126, code)
+    return (code | np.where(x < 0, 0x80, 0)).astype(np.uint8)
+
+
+def encode(x, dt: str) -> np.ndarray:
+    if dt == "f32":
+        return np.ascontiguousarray(x, dtype=np.float32)
+    if dt == "bf16":
+        return f32_to_bf16(x)
+    raise ValueError(dt)
+
+
+def decode_f32(a, dt: str) -> np.ndarray:
+    """Decode an f32/bf16 encoded array to float32 (used by the generator to place forced maxima)."""
+    return np.asarray(a, np.float32) if dt == "f32" else bf16_to_f32(a)
+
+
+# ----------------------------------------------------------------------------------------------------
+# trees
+# ----------------------------------------------------------------------------------------------------
+def level_sizes(T: int, branching) -> list[int]:
+    depth = len(branching)
+    rem = T - 1
+    sizes = [1]
+    for d in range(1, depth + 1):
+        n = min(sizes[-1] * branching[d - 1], rem - (depth - d))
+        if n < 1:
+            raise ValueError(f"tree T={T} branching={branching} cannot reach depth {depth}")
+        sizes.append(n)
+        rem -= n
+    if rem != 0:
+        raise ValueError(f"tree T={T} branching={branching} leaves {rem} nodes unplaced")
+    return sizes
+
+
+def make_tree(rng: np.random.Generator, T: int, branching) -> np.ndarray:
+    """Topological parent array (int32 [T], parent[0] = -1), BFS-numbered by (parent, rank)."""
+    sizes = level_sizes(T, branching)
+    parent = [-1]
+    prev = [0]
+    for d in range(1, len(sizes)):
+        k = branching[d - 1]
+        cand = [(p, r) for p in prev for r in range(k)]
+        pick = np.sort(rng.choice(len(cand), size=sizes[d], replace=False))
+        prev = []
+        for i in pick:
+            parent.append(cand[i][0])
+            prev.append(len(parent) - 1)
+    return np.asarray(parent, np.int32)
+
+
+def chain_tree(T: int) -> np.ndarray:
+    return np.arange(-1, T - 1, dtype=np.int32)
+
+
+def star_tree(T: int) -> np.ndarray:
+    p = np.zeros(T, np.int32)
+    p[0] = -1
+    return p
+
+
+def children_of(parent: np.ndarray) -> list[list[int]]:
+    ch = [[] for _ in range(len(parent))]
+    for i in range(1, len(parent)):
+        ch[int(parent[i])].append(i)
+    return ch
+
+
+# ----------------------------------------------------------------------------------------------------
+# verify workloads (attention + acceptance)
+# ----------------------------------------------------------------------------------------------------
+@dataclass
+class Verify:
+    B: int
+    T: int
+    Hq: int
+    Hkv: int
+    D: int
+    kv_cap: int
+    V: int
+    q_dt: str
+    kv_dt: str
+    logit_dt: str
+    q: np.ndarray                 # [B,T,Hq,D]
+    k: np.ndarray                 # [B,Hkv,kv_cap,D]
+    v: np.ndarray                 # [B,Hkv,kv_cap,D]
+    k_scale: np.ndarray | None    # [Hkv] float32 (e4m3 only)
+    v_scale: np.ndarray | None
+    kv_len: np.ndarray            # [B] int32 prefix length L_b; tree K/V at L_b .. L_b+T-1
+    parent: np.ndarray            # [B,T] int32
+    tokens: np.ndarray            # [B,T] int32, tokens[b,0] = root token
+    target_logits: np.ndarray     # [B,T,V]
+    draft_logits: np.ndarray | None
+    uniforms: np.ndarray | None   # [B,T] uint32
+    temperature: float
+    name: str = ""
+    meta: dict = field(default_factory=dict)
+
+
+def _encode_kv(x, dt, kv_len, T, junk):
+    """Encode a [B,Hkv,cap,D] float32 cache; positions >= kv_len+T hold junk (random, or NaN patterns)."""
+    B, Hkv, cap, D = x.shape
+    valid = (np.arange(cap)[None, :] < (kv_len[:, None] + T))  # [B,cap]
+    scale = None
+    if dt == "e4m3":
+        amax = np.max(np.abs(np.where(valid[:, None, :, None], x, 0.0)), axis=(0, 2, 3))
+        scale = (np.maximum(amax, 1e-30) / 448.0).astype(np.float32)
+        enc = f32_to_e4m3(x / scale[None, :, None, None])
+        if junk == "nan":
+            enc = np.where(valid[:, None, :, None], enc, np.uint8(0x7F))
+        return enc, scale
+    enc = encode(x, dt)
+    if junk == "nan":
+        nan = np.float32(np.nan) if dt == "f32" else np.uint16(0x7FC0)
+        enc = np.where(valid[:, None, :, None], enc, nan).astype(enc.dtype)
+    return enc, scale
+
+
+def _force_max(row_f32: np.ndarray, tok: int) -> float:
+    """Value that makes `tok` the unique maximum of the row after encoding (max + 1)."""
+    return float(np.max(row_f32)) + 1.0
+
+
+def make_verify(seed: int, *, B: int, T: int, Hq: int, Hkv: int, D: int, L: tuple[int, int], V: int,
+                q_dt: str = "bf16", kv_dt: str = "bf16", logit_dt: str = "bf16", tree="chain",
+                mode: str = "greedy", temperature: float = 0.0, force_p: float = 0.7, sigma: float = 3.0,
+                rho: float = 0.8, kv_cap: int | None = None, junk: str = "randn", name: str = "",
+                with_attn: bool = True) -> Verify:
+    """Draw one verify batch.
+
+    mode 'greedy' / 'onehot': at every internal node, with probability force_p one uniformly chosen child
+    carries the token that is made the row's unique maximum (its logit is set to the row max + 1); otherwise
+    a token outside the children is made the maximum.  Children's tokens are distinct.
+    mode 'prob': draft logits z_q = sigma*e1 and target logits z_p = sigma*(rho*e1 + sqrt(1-rho^2)*e2);
+    each child's token is drawn from softmax(z_q(parent)/temperature) by the Gumbel-max trick.
+    """
+    (s_tree, s_len, s_q, s_k, s_v, s_lp, s_lq, s_tok, s_u, s_force, s_junk) = rng_streams(seed, 11)
+    if tree == "chain":
+        parents = np.stack([chain_tree(T) for _ in range(B)])
+    elif tree == "star":
+        parents = np.stack([star_tree(T) for _ in range(B)])
+    else:
+        parents = np.stack([make_tree(s_tree, T, tree) for _ in range(B)])
+    lo, hi = L
+    kv_len = s_len.integers(lo, hi, size=B, endpoint=True).astype(np.int32)
+    cap = int(kv_cap if kv_cap is not None else hi + T)
+    if with_attn:
+        q = encode(s_q.standard_normal(size=(B, T, Hq, D), dtype=np.float32), q_dt)
+        kx = s_k.standard_normal(size=(B, Hkv, cap, D), dtype=np.float32)
+        vx = s_v.standard_normal(size=(B, Hkv, cap, D), dtype=np.float32)
+        k, k_scale = _encode_kv(kx, kv_dt, kv_len, T, junk)
+        v, v_scale = _encode_kv(vx, kv_dt, kv_len, T, junk)
+        del kx, vx
+    else:
+        q = k = v = None
+        k_scale = v_scale = None
+
+    tokens = np.zeros((B, T), np.int32)
+    tokens[:, 0] = s_tok.integers(0, V, size=B)
+    draft = None
+    uniforms = None
+    if mode == "prob":
+        e1 = s_lq.standard_normal(size=(B, T, V), dtype=np.float32)
+        e2 = s_lp.standard_normal(size=(B, T, V), dtype=np.float32)
+        zq = encode(sigma * e1, logit_dt)
+        zp = encode(sigma * (rho * e1 + math.sqrt(1.0 - rho * rho) * e2), logit_dt)
+        del e1, e2
+        zq_f = decode_f32(zq, logit_dt)
+        tinv = 1.0 / temperature
+        for b in range(B):
+            ch = children_of(parents[b])
+            for p in range(T):
+                if not ch[p]:
+                    continue
+                g = s_tok.gumbel(size=(len(ch[p]), V))
+                picks = np.argmax(zq_f[b, p][None, :].astype(np.float64) * tinv + g, axis=1)
+                for c, x in zip(ch[p], picks):
+                    tokens[b, c] = x
+        target, draft = zp, zq
+    else:
+        zf = (sigma * s_lp.standard_normal(size=(B, T, V), dtype=np.float32))
+        target = encode(zf, logit_dt)
+        tf = decode_f32(target, logit_dt).copy()
+        for b in range(B):
+            ch = children_of(parents[b])
+            for p in range(T):
+                if not ch[p]:
+                    continue
+                toks = s_tok.choice(V, size=len(ch[p]) + 1, replace=False)
+                for c, x in zip(ch[p], toks[:-1]):
+                    tokens[b, c] = x
+                if s_force.random() < force_p:
+                    star = int(tokens[b, ch[p][s_force.integers(0, len(ch[p]))]])
+                else:
+                    star = int(toks[-1])
+                tf[b, p, star] = _force_max(tf[b, p], star)
+        target = encode(tf, logit_dt)
+        del tf, zf
+    if mode in ("prob", "onehot"):
+        uniforms = s_u.integers(0, 2 ** 32, size=(B, T), dtype=np.uint32)
+    return Verify(B=B, T=T, Hq=Hq, Hkv=Hkv, D=D, kv_cap=cap, V=V, q_dt=q_dt, kv_dt=kv_dt,
+                  logit_dt=logit_dt, q=q, k=k, v=v, k_scale=k_scale, v_scale=v_scale, kv_len=kv_len,
+                  parent=parents, tokens=tokens, target_logits=target, draft_logits=draft,
+                  uniforms=uniforms, temperature=float(temperature if mode != "greedy" else 0.0),
+                  name=name, meta=dict(mode=mode, tree=tree, L=L, seed=seed))
+
+
+# ----------------------------------------------------------------------------------------------------
+# loss workloads
+# ----------------------------------------------------------------------------------------------------
+@dataclass
+class LossBatch:
+    N: int
+    T: int
+    V: int
+    logits: np.ndarray    # [N*T, V] bf16 bits
+    tokens: np.ndarray    # [N,T] int32
+    parent: np.ndarray    # [N,T] int32
+    labels: np.ndarray    # [N,T] int32 (target argmax after each node)
+    name: str = ""
+    meta: dict = field(default_factory=dict)
+
+
+def make_loss(seed: int, *, N: int, T: int, V: int, tree=(4, 3, 2, 1, 1), sigma: float = 3.0,
+              accept_frac: float = 0.45, name: str = "") -> LossBatch:
+    """Logged traces: at each internal node, with probability pi = min(1, accept_frac*(T-1)/n_internal)
+    one uniformly chosen child carries the parent's label; the other children carry distinct tokens that
+    differ from the label."""
+    (s_tree, s_z, s_lab, s_tok, s_pi) = rng_streams(seed, 5)
+    if tree == "chain":
+        parents = np.stack([chain_tree(T) for _ in range(N)])
+    else:
+        parents = np.stack([make_tree(s_tree, T, tree) for _ in range(N)])
+    logits = f32_to_bf16(sigma * s_z.standard_normal(size=(N * T, V), dtype=np.float32))
+    labels = s_lab.integers(0, V, size=(N, T)).astype(np.int32)
+    tokens = np.zeros((N, T), np.int32)
+    tokens[:, 0] = s_tok.integers(0, V, size=N)
+    for n in range(N):
+        ch = children_of(parents[n])
+        n_int = sum(1 for c in ch if c)
+        pi = min(1.0, accept_frac * (T - 1) / max(n_int, 1))
+        for p in range(T):
+            if not ch[p]:
+                continue
+            lab = int(labels[n, p])
+            pool = s_tok.choice(V - 1, size=len(ch[p]), replace=False)
+            others = [int(x) + (1 if x >= lab else 0) for x in pool]   # distinct, never the label
+            for c, x in zip(ch[p], others):
+                tokens[n, c] = x
+            if s_pi.random() < pi:
+                tokens[n, ch[p][s_pi.integers(0, len(ch[p]))]] = lab
+    return LossBatch(N=N, T=T, V=V, logits=logits, tokens=tokens, parent=parents, labels=labels,
+                     name=name, meta=dict(tree=tree, seed=seed))
+
+
+# ----------------------------------------------------------------------------------------------------
+# named workloads (the shapes of the pages' serving setups; see the design doc for the recipe)
+# ----------------------------------------------------------------------------------------------------
+WORKLOADS = {
+    # B=1, chain of 5 drafts, 4/1 heads, D=64, fp32 QKV, L=128, fp32 logits V=1024, greedy
+    "tiny_chain": dict(kind="verify", B=1, T=6, Hq=4, Hkv=1, D=64, L=(128, 128), V=1024, q_dt="f32",
+                       kv_dt="f32", logit_dt="f32", tree="chain", mode="greedy", force_p=0.7, sigma=3.0),
+    # Llama3-8B-shaped EAGLE tree: B=8, 60 nodes depth 6 (4/3/2/2/1/1), 32/8 heads, D=128, L in [2048,8192]
+    "llama3_8b_tree": dict(kind="verify", B=8, T=60, Hq=32, Hkv=8, D=128, L=(2048, 8192), V=128256,
+                           q_dt="bf16", kv_dt="bf16", logit_dt="bf16", tree=(4, 3, 2, 2, 1, 1),
+                           mode="greedy", force_p=0.65, sigma=3.0),
+    # Qwen3-8B-shaped stochastic chain: B=32, lookahead 5, L in [512,4096], V=151936, T=1.0
+    "qwen3_8b_stochastic": dict(kind="verify", B=32, T=6, Hq=32, Hkv=8, D=128, L=(512, 4096), V=151936,
+                                q_dt="bf16", kv_dt="bf16", logit_dt="bf16", tree="chain", mode="prob",
+                                temperature=1.0, sigma=2.5, rho=0.8),
+    # online-training loss: 64 traces x 32 nodes, depth 5 (4/3/2/1/1), V=128256
+    "loss_batch": dict(kind="loss", N=64, T=32, V=128256, tree=(4, 3, 2, 1, 1), sigma=3.0,
+                       accept_frac=0.45),
+    # FP8 long context: B=128, 64 nodes depth 7 (4/3/2/2/1/1/1), 64/8 heads, e4m3 KV, L in [8192,32768]
+    "fp8_long_context": dict(kind="verify", B=128, T=64, Hq=64, Hkv=8, D=128, L=(8192, 32768), V=151936,
+                             q_dt="bf16", kv_dt="e4m3", logit_dt="bf16", tree=(4, 3, 2, 2, 1, 1, 1),
+                             mode="greedy", force_p=0.7, sigma=3.0),
+}
+
+
+def make_workload(name: str, seed: int = 0, **overrides):
+    cfg = dict(WORKLOADS[name])
+    cfg.update(overrides)
+    kind = cfg.pop("kind")
+    if kind == "loss":
+        return make_loss(seed, name=name, **cfg)
+    return make_verify(seed, name=name, **cfg)
