@@ -1,0 +1,361 @@
+"""Benchmark: verified tree nodes per second of one verification step (tree attention + acceptance).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl sv|reference] [--workload NAME]
+
+A step is one pass of the verify path over one batch: sv_tree_attn over every node of every request,
+then sv_accept (walk + bonus).  The default workload is the Llama3-8B-shaped EAGLE tree batch
+(B=8, 60-node trees, 32/8 heads, D=128, bf16, KV prefixes of 2048..8192, vocabulary 128256, greedy).
+value = B*T*world / device time per step (CUDA events on the launching stream, L2 flushed between steps
+by a 256 MB write outside the timed events).  e2e = the same metric through the C ABI with the step's
+inputs copied from pinned host memory and its outputs copied back inside the timed region.  Under
+torchrun every rank verifies its own batch (weak scaling, no collective on the data path).
+--impl reference times the CPU oracle on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+METRIC = "verified tree nodes/s on 1 GB300 (attn+accept); % of HBM roofline achieved"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["sv", "reference"], default="sv")
+    ap.add_argument("--workload", default="llama3_8b_tree")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------------------------------ algorithmic bytes
+ES = {"f32": 4, "bf16": 2, "e4m3": 1}
+
+
+def attn_bytes(w):
+    """Bytes the method must move: K and V of every allowed position (prefix + tree block) once per kv head,
+    Q in, O out, lse out, plus the small int arrays."""
+    kv = int(np.sum(w.kv_len.astype(np.int64) + w.T)) * w.Hkv * w.D * 2 * ES[w.kv_dt]
+    qo = 2 * w.B * w.T * w.Hq * w.D * ES[w.q_dt]
+    return kv + qo + w.B * w.T * w.Hq * 4 + w.B * (w.T + 1) * 4
+
+
+def accept_bytes(w):
+    rows = w.B * w.T * (2 if (w.temperature > 0 and w.draft_logits is not None) else 1)
+    return rows * w.V * ES[w.logit_dt] + w.B * w.T * 4 * 6
+
+
+# ------------------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------ CPU oracle timing
+def cpu_oracle_sample(w, budget_s: float):
+    """Time the oracle (as it stands) on whole requests of the workload until the budget is spent.
+    Returns (nodes per second, threads, description)."""
+    import oracle
+    from speculative_decoding_tree_verify_gb300 import workloads as W
+    done, t_total = 0, 0.0
+    for b in range(w.B):
+        sub = W.Verify(B=1, T=w.T, Hq=w.Hq, Hkv=w.Hkv, D=w.D, kv_cap=w.kv_cap, V=w.V, q_dt=w.q_dt, kv_dt=w.kv_dt,
+                       logit_dt=w.logit_dt, q=w.q[b:b + 1], k=w.k[b:b + 1], v=w.v[b:b + 1], k_scale=w.k_scale,
+                       v_scale=w.v_scale, kv_len=w.kv_len[b:b + 1], parent=w.parent[b:b + 1],
+                       tokens=w.tokens[b:b + 1], target_logits=w.target_logits[b:b + 1],
+                       draft_logits=None if w.draft_logits is None else w.draft_logits[b:b + 1],
+                       uniforms=None if w.uniforms is None else w.uniforms[b:b + 1], temperature=w.temperature)
+        t0 = time.perf_counter()
+        oracle.tree_attn_w(sub)
+        oracle.accept_w(sub)
+        t_total += time.perf_counter() - t0
+        done += 1
+        if t_total >= budget_s:
+            break
+    return done * w.T / t_total, oracle.num_threads(), f"{done} of {w.B} requests (all {w.T} nodes, all heads)"
+
+
+# ------------------------------------------------------------------------------------------ profiles
+def traffic_from_profile(kernel_src: Path, workload: str):
+    """DRAM traffic per launch from a committed ncu summary, valid only while the kernel source is unchanged."""
+    p = ROOT / "profiles" / "traffic.json"
+    if not p.exists():
+        return None
+    d = json.loads(p.read_text()).get(workload)
+    if not d:
+        return None
+    h = hashlib.sha256(kernel_src.read_bytes()).hexdigest()[:16]
+    return d["traffic_bytes_per_launch"] if d.get("source_sha") == h else None
+
+
+# ------------------------------------------------------------------------------------------ main arms
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from speculative_decoding_tree_verify_gb300 import workloads as W
+    w = W.make_workload(args.workload, seed=args.seed)
+    per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    vals = []
+    for i in range(args.warmup + args.steps):
+        v, cores, desc = cpu_oracle_sample(w, per_step)
+        if i >= args.warmup:
+            vals.append(v)
+    value = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "nodes/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * w.B * w.T / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "B": w.B, "T": w.T, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                       "V": w.V, "kv_dt": w.kv_dt, "sample": desc},
+            "cpu_baseline": {"value": value, "unit": "nodes/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "nodes/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_sv(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from speculative_decoding_tree_verify_gb300 import sv
+    from speculative_decoding_tree_verify_gb300 import workloads as W
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = W.make_workload(args.workload, seed=args.seed + rank)
+
+    def to_dev(a, pin=False):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        elif a.dtype == np.uint32:
+            a = a.view(np.int32)
+        t = torch.from_numpy(a)
+        return t.pin_memory() if pin else t.to(dev)
+
+    names = ("q", "k", "v", "k_scale", "v_scale", "kv_len", "parent", "tokens", "target_logits", "draft_logits",
+             "uniforms")
+    host = {k: to_dev(getattr(w, k), pin=True) for k in names if getattr(w, k) is not None}
+    d = {k: t.to(dev) for k, t in host.items()}
+    for k in names:
+        d.setdefault(k, None)
+    B, T, V = w.B, w.T, w.V
+    i32 = dict(dtype=torch.int32, device=dev)
+    out = torch.empty_like(d["q"])
+    lse = torch.empty((B, T, w.Hq), dtype=torch.float32, device=dev)
+    st_a = torch.empty((B,), **i32)
+    acc = dict(accept_len=torch.empty((B,), **i32), path=torch.empty((B, T), **i32),
+               out_tokens=torch.empty((B, T), **i32), bonus=torch.empty((B,), **i32),
+               status=torch.empty((B,), **i32))
+    ws_attn_n = sv.workspace_size(sv.OP_TREE_ATTN, B, T, w.Hq, w.Hkv, w.D, w.kv_cap, 0)
+    ws_attn = torch.empty(max(ws_attn_n, 256), dtype=torch.uint8, device=dev)
+    ws_acc = torch.empty(max(sv.workspace_size(sv.OP_ACCEPT, B, T, V=V), 256), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    logits = d["target_logits"]
+
+    def step():
+        sv.tree_attn(d["q"], d["k"], d["v"], d["kv_len"], d["parent"], out, k_scale=d.get("k_scale"),
+                     v_scale=d.get("v_scale"), lse=lse, status=st_a, workspace=ws_attn)
+        ev_mid = torch.cuda.Event(enable_timing=True)
+        ev_mid.record(stream)
+        sv.accept(logits, d["tokens"], d["parent"], acc["accept_len"], acc["path"], acc["out_tokens"],
+                  acc["bonus"], draft_logits=d["draft_logits"], temperature=w.temperature, uniforms=d["uniforms"],
+                  status=acc["status"], workspace=ws_acc)
+        return ev_mid
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert (st_a == 0).all() and (acc["status"] == 0).all(), "verify step reported a per-request error"
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    evs = []
+    with ClockSampler(local_rank) as clk:
+        for _ in range(args.steps):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e2 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            e1 = step()
+            e2.record(stream)
+            evs.append((e0, e1, e2))
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t_attn = sum(e0.elapsed_time(e1) for e0, e1, _ in evs) / args.steps
+    t_acc = sum(e1.elapsed_time(e2) for _, e1, e2 in evs) / args.steps
+    ms = t_attn + t_acc
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = B * T * world / (ms * 1e-3)
+
+    # end to end through the C ABI: inputs from pinned host memory, outputs back, inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        res_h = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in acc.items() if k != "status"}
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_h.numel() * out_h.element_size() + sum(t.numel() * t.element_size() for t in res_h.values())
+
+        def e2e_step():
+            for k, t in host.items():
+                d[k].copy_(t, non_blocking=True)
+            step()
+            out_h.copy_(out, non_blocking=True)
+            for k, t in res_h.items():
+                t.copy_(acc[k], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(3, args.steps // 2)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = t0.elapsed_time(t1) / n_e2e
+        if world > 1:
+            t = torch.tensor([ms_e2e], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms_e2e = float(t.item())
+        e2e = {"value": B * T * world / (ms_e2e * 1e-3), "unit": "nodes/s", "h2d_bytes_per_step": int(h2d) * world,
+               "d2h_bytes_per_step": int(d2h) * world, "ms_per_step": ms_e2e}
+
+    if rank != 0:
+        return
+    peak, peak_kind = peaks()
+    ab, cb = attn_bytes(w), accept_bytes(w)
+    # the dominant kernel is the one with the larger share of the step
+    if t_attn >= t_acc:
+        dom, byt, t_dom, src = "tree_attn", ab, t_attn, ROOT / "speculative_decoding_tree_verify_gb300/csrc/attn_simt.cu"
+    else:
+        dom, byt, t_dom, src = "accept", cb, t_acc, ROOT / "speculative_decoding_tree_verify_gb300/csrc/accept.cu"
+    achieved = byt / (t_dom * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
+                "unit": "GB/s", "frac": achieved / peak, "algorithmic_bytes_per_launch": byt,
+                "traffic": traffic_from_profile(src, args.workload),
+                "step_frac": (ab + cb) / (ms * 1e-3) / 1e9 / peak}
+    cpu = None
+    if not args.no_cpu_baseline:
+        v, cores, desc = cpu_oracle_sample(w, args.cpu_seconds)
+        cpu = {"value": v, "unit": "nodes/s", "cores": cores, "kind": "oracle", "sample": desc}
+    launches_per_step = (1 if ws_attn_n == 0 else 3) + 2
+    line = {"metric": METRIC, "value": value, "unit": "nodes/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.q_dt, "data": "synthetic",
+            "config": {"workload": args.workload, "B": B, "T": T, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D, "V": V,
+                       "kv_dt": w.kv_dt, "logit_dt": w.logit_dt, "mode": w.meta["mode"],
+                       "mean_kv_len": float(np.mean(w.kv_len)), "l2": "flushed by a 256 MB write between steps",
+                       "parallelism": f"replicas{world}" if world > 1 else "single"},
+            "components": {"attn_ms": t_attn, "accept_ms": t_acc, "attn_bytes": ab, "accept_bytes": cb},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps, "clocks": clk.summary(),
+            "mean_accept_len": float(acc["accept_len"].float().mean().item())}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_sv(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.path.insert(0, str(ROOT))
+    main()

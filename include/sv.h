@@ -1,0 +1,163 @@
+/*
+ * sv.h -- C ABI of libsv.so: speculative tree verification on one GB300 (sm_103a).
+ *
+ * Three hot-path calls sit under a speculative-decoding server's verify step and under its online draft
+ * trainer:
+ *   sv_tree_attn  tree-masked GQA attention of every draft-tree node over the request's KV prefix and its
+ *                 own ancestors ("Aurora" post, section 2: a custom attention mask that follows the
+ *                 speculative tree's causal structure so all branches go through one batched pass);
+ *   sv_accept     the target's verification of the draft tree: greedy argmax matching or rejection
+ *                 sampling, giving the acceptance length (TIDE evaluation section: draft tokens accepted
+ *                 per verification step), the accepted path and the target's own next token;
+ *   sv_loss       the draft-training signal from logged trees ("Aurora" post, section 2: cross-entropy on
+ *                 accepted tokens plus a rejection loss on rejected branches), taken here as
+ *                 -log q(accepted token) and -log(1 - q(rejected token)), with its gradient.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Every pointer argument except the host scalars is DEVICE memory owned by the caller.  The library
+ *    allocates nothing, keeps no state between calls and never synchronises the stream.
+ *  - Work is enqueued on `stream` and runs asynchronously; outputs are valid once the stream reaches the
+ *    call.  Calls on different streams may overlap only if they use different workspaces and outputs.
+ *  - A draft tree is a parent array int32 [T] per request: parent[0] = -1 (node 0 is the root, the last
+ *    committed token) and 0 <= parent[i] < i for i >= 1 (topological order).  Siblings are ordered by
+ *    node id, which is the draft's rank order.  T <= 64.
+ *  - Errors in host-visible arguments (sizes, dtypes, NULL or misaligned pointers, a workspace that is
+ *    too small) are returned synchronously and nothing is launched.  Errors in device data (a malformed
+ *    parent array, a token >= V, kv_len + T > kv_cap, non-finite logits) are reported per request in the
+ *    optional status array with the same codes; the call still returns SV_OK.  No kernel ever traps.
+ *  - Alignment: tensors read with 128-bit loads (q, caches, logits, gradient) must be 16-byte aligned and
+ *    their row lengths (D or V elements) must keep every row 16-byte aligned, otherwise SV_ERR_UNSUPPORTED.
+ *    int32 / float arrays must be 4-byte aligned.
+ *  - SV_ERR_CUDA means a launch failed; cudaGetLastError() holds the CUDA code.
+ */
+#ifndef SV_H
+#define SV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* sv_stream_t; /* == cudaStream_t; NULL is the legacy default stream */
+
+typedef enum {
+    SV_OK = 0,
+    SV_ERR_INVALID_ARG = 1,      /* bad size, NULL pointer, or (per request) token/kv_len out of range  */
+    SV_ERR_BAD_TREE = 2,         /* (per request) parent array is not a topological tree rooted at 0     */
+    SV_ERR_TREE_TOO_LARGE = 3,   /* T > 64                                                               */
+    SV_ERR_UNSUPPORTED = 4,      /* dtype / shape / alignment combination not provided                   */
+    SV_ERR_NONFINITE = 5,        /* (per request) NaN or Inf in a logit row the call reads               */
+    SV_ERR_TIMEOUT = 6,          /* (per request) a bounded device-side wait gave up                     */
+    SV_ERR_CUDA = 7,             /* a CUDA launch failed                                                  */
+    SV_ERR_WORKSPACE = 8         /* workspace NULL or smaller than sv_workspace_size()                   */
+} sv_status;
+
+typedef enum { SV_F32 = 0, SV_BF16 = 1, SV_E4M3 = 2 } sv_dtype;
+
+typedef enum { SV_OP_TREE_ATTN = 0, SV_OP_ACCEPT = 1, SV_OP_LOSS = 2 } sv_op;
+
+/* Human-readable name of a status code (static storage). */
+const char* sv_status_string(sv_status s);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int sv_version(void);
+
+/*
+ * Bytes of device workspace a call needs (0 if none).  Arguments that do not apply to `op` are ignored:
+ *   SV_OP_TREE_ATTN: B, T, Hq, Hkv, D, kv_cap      SV_OP_ACCEPT: B (= rows/T), T, V      SV_OP_LOSS: B (= N), T, V
+ * The result is an upper bound that does not depend on device data, so it can be computed once.
+ */
+size_t sv_workspace_size(sv_op op, int B, int T, int Hq, int Hkv, int D, int kv_cap, int V);
+
+/*
+ * sv_tree_attn -- tree-masked grouped-query attention for one verification step.
+ *
+ * For request b, node i (0 <= i < T) and query head h, with kv head hk = h / (Hq / Hkv):
+ *     allowed(b, i) = { 0 .. kv_len[b]-1 }  U  { kv_len[b] + a : a is i, an ancestor of i, or the root }
+ *     out[b,i,h,:]  = sum_{j in allowed} softmax_j( sm_scale * <q[b,i,h,:], K[b,hk,j,:]> ) * V[b,hk,j,:]
+ *     lse[b,i,h]    = log sum_{j in allowed} exp( sm_scale * <q, K_j> )            (natural log)
+ * The tree's own K/V (node a) sit in the cache at position kv_len[b] + a, already written by the caller.
+ *
+ *   q        [B, T, Hq, D]        q_dt  (SV_F32 or SV_BF16)
+ *   k_cache  [B, Hkv, kv_cap, D]  kv_dt (SV_F32, SV_BF16, or SV_E4M3 with per-kv-head scales)
+ *   v_cache  [B, Hkv, kv_cap, D]  kv_dt
+ *   k_scale, v_scale  float [Hkv]: real value = decoded E4M3 * scale; required for SV_E4M3, else ignored
+ *   kv_len   int32 [B]  prefix length L_b; requires 0 <= L_b and L_b + T <= kv_cap (else status 1)
+ *   parent   int32 [B, T]
+ *   sm_scale float; 0 selects 1/sqrt(D)
+ *   out      [B, T, Hq, D] in q_dt
+ *   lse      float [B, T, Hq] or NULL
+ *   status   int32 [B] or NULL; a failed request's out/lse rows are zero
+ *   workspace / ws_bytes: at least sv_workspace_size(SV_OP_TREE_ATTN, ...) bytes, 256-byte aligned
+ * Cache positions >= kv_len[b] + T are never used, whatever they hold (NaN included).
+ * Shapes: 1 <= T <= 64, Hq % Hkv == 0, D in {64, 128} for the tensor-core path (other D up to 256 run
+ * on the CUDA-core path), Hq / Hkv * T <= 512.
+ */
+sv_status sv_tree_attn(int B, int T, int Hq, int Hkv, int D, int kv_cap, sv_dtype q_dt, sv_dtype kv_dt,
+                       const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                       const float* v_scale, const int32_t* kv_len, const int32_t* parent, float sm_scale,
+                       void* out, float* lse, int32_t* status, void* workspace, size_t ws_bytes,
+                       sv_stream_t stream);
+
+/*
+ * sv_accept -- verify one batch of draft trees against the target's per-node logits.
+ *
+ * Row i of request b (target_logits[b, i, :]) is the target's next-token logits after node i.  The walk
+ * starts at the root; at node `cur` its children are tried in ascending node id:
+ *   greedy (temperature == 0): the first child whose token equals argmax(row cur) (lowest index on ties)
+ *       is accepted; if none, the walk stops and bonus = argmax(row cur).
+ *   stochastic (temperature > 0): standard speculative sampling, accept with probability min(1, p/q) and
+ *       otherwise continue with the residual norm(max(0, p - q)), under an exact integer contract so
+ *       results are reproducible bit for bit:
+ *         y = fp32(z) * invT, invT = (float)(1 / (double)temperature); m = max y; t = (y - m) * log2(e);
+ *         W = 0 if t < -24, else floor(P(t - n) * 2^(24 + n)), n = rint(t), P the degree-7 Horner
+ *         polynomial with coefficients fp32((ln 2)^j / j!) evaluated with fma;  S = sum W  (p ~ W / S).
+ *       child c with token x is accepted iff  U_c * Wq(x) * S'_p  <  2^32 * W'_p(x) * S_q   (128-bit),
+ *       U_c = uniforms[b, c].  On rejection, W'_p(k) <- floor(max(0, W'_p(k) S_q - Wq(k) S'_p) / S_q).
+ *       draft_logits == NULL means one-hot proposals (q = delta of the child's token: rejection zeroes
+ *       that token).  When the walk stops, the bonus token is the smallest j whose prefix sum of the
+ *       final weights exceeds floor(uniforms[b, 0] * R / 2^32), R = sum of the weights: the residual after
+ *       rejections (or the row itself when it is empty) or, at a node with no children, the node's row.
+ *   Outputs (for a failed request: accept_len = bonus = -1, path/out_tokens all -1):
+ *   accept_len int32 [B]     number of accepted DRAFT tokens (root and bonus not counted)
+ *   path       int32 [B, T]  accepted node ids in order, then -1
+ *   out_tokens int32 [B, T]  tokens of the accepted nodes, then the bonus token, then -1
+ *   bonus      int32 [B]
+ *   argmax     int32 [B, T] or NULL: argmax of every target row (first index; -1 if the row is not finite)
+ *   status     int32 [B] or NULL
+ *   target_logits / draft_logits: [B, T, V] in logit_dt (SV_F32 or SV_BF16); the draft row of a node is
+ *       its proposal distribution for the node's children.  tokens int32 [B, T] (tokens[b,0] unused).
+ *   uniforms uint32 [B, T], raw 32-bit uniforms; required iff temperature > 0.
+ *   workspace: at least sv_workspace_size(SV_OP_ACCEPT, B, T, 0, 0, 0, 0, V) bytes.
+ */
+sv_status sv_accept(int B, int T, int V, sv_dtype logit_dt, const void* target_logits,
+                    const void* draft_logits, const int32_t* tokens, const int32_t* parent, float temperature,
+                    const uint32_t* uniforms, int32_t* accept_len, int32_t* path, int32_t* out_tokens,
+                    int32_t* bonus, int32_t* argmax, int32_t* status, void* workspace, size_t ws_bytes,
+                    sv_stream_t stream);
+
+/*
+ * sv_loss -- acceptance + rejection loss of the draft over N logged trees, and its gradient.
+ *
+ * Row (n, p) of draft_logits ([N*T, V], bf16) is the draft's logits after node p of trace n; q_p is its
+ * softmax.  For every non-root node j with parent p and token x = tokens[n, j]:
+ *     accepted  (x == labels[n, p], the target's token after p):  term = -log q_p(x)
+ *     rejected  (otherwise):                                       term = -log(1 - q_p(x)), q_p(x) <= 1 - 1e-6
+ * loss = (sum of accepted terms + sum of rejected terms) / n_terms,  n_terms = N * (T - 1).
+ *   row_loss  float [N*T]   sum of the terms of row p's children (0 for leaves)
+ *   sums      float [3]     { sum accepted, sum rejected, n_terms } (fixed-order reduction: deterministic)
+ *   grad      bf16 [N*T, V] d loss / d draft_logits (leaf rows are zero), or NULL to skip it
+ *   status    int32 [N] or NULL; a failed trace contributes no terms and a zero gradient
+ *   workspace: at least sv_workspace_size(SV_OP_LOSS, N, T, 0, 0, 0, 0, V) bytes.
+ */
+sv_status sv_loss(int N, int T, int V, const void* draft_logits, const int32_t* tokens,
+                  const int32_t* parent, const int32_t* labels, float* row_loss, float* sums, void* grad,
+                  int32_t* status, void* workspace, size_t ws_bytes, sv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SV_H */

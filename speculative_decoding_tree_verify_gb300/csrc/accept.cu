@@ -1,0 +1,509 @@
+// accept.cu -- verification of draft trees against the target's per-node logits.
+//
+// The target checks every draft node in one pass ("Aurora" post, section 2; TIDE overview) and the
+// acceptance length is the number of draft tokens accepted per verification step (TIDE evaluation).
+//
+// Kernel 1 (rows): one thread-block cluster of CL CTAs per logit row, each CTA one contiguous slice of
+//   the vocabulary, 128-bit loads.  Greedy: (max, first index) -> argmax.  Stochastic: max of y = z*invT,
+//   then the fixed-point weight sum S of the integer contract.  Partial results meet in distributed
+//   shared memory; no global partials, one HBM read of every row.
+// Kernel 2 (walk): one cluster per request.  Greedy: a single thread follows the argmax matches.
+//   Stochastic: every thread of the cluster runs the same walk on broadcast scalars; the residual sums and
+//   the bonus draw are cluster-wide passes over the stopping row only.
+//
+// Integer contract (stated in include/sv.h, implemented here from that text):
+//   y = fp32(z) * invT;  m = max y;  t = (y - m) * log2(e);  W = 0 if t < -24 else
+//   floor(P(t - rint(t)) * 2^(24 + rint(t))), P(f) = sum_j fp32((ln 2)^j / j!) f^j (degree 7, Horner, fma);
+//   accept child c (token x) iff U_c * Wq(x) * S'_p < 2^32 * W'_p(x) * S_q; on rejection
+//   W'_p(k) <- floor(max(0, W'_p(k) * S_q - Wq(k) * S'_p) / S_q); bonus = smallest j with
+//   prefix_sum(j) > floor(U_0 * R / 2^32).
+#include <cooperative_groups.h>
+
+#include "sv_internal.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace sv {
+namespace {
+
+typedef unsigned long long u64;
+typedef unsigned __int128 u128;
+
+constexpr int kRowThreads = 256;
+constexpr int kWalkThreads = 512;
+constexpr int kMaxCluster = 8;
+
+struct RowStat {
+    float zmax;   // max of z
+    int arg;      // first index of the max of z, -1 if the row holds a non-finite z
+    float ymax;   // max of y = z * invT (stochastic)
+    int fin;      // row usable: z finite (greedy) / y finite (stochastic)
+    u64 S;        // sum of fixed-point weights (stochastic)
+};
+
+// ------------------------------------------------------------------------------------ the contract
+__device__ __forceinline__ float fx_exp2_poly(float f) {
+    float p = 0x1.ffcbfcp-17f;
+    p = __fmaf_rn(p, f, 0x1.430912p-13f);
+    p = __fmaf_rn(p, f, 0x1.5d87fep-10f);
+    p = __fmaf_rn(p, f, 0x1.3b2ab6p-7f);
+    p = __fmaf_rn(p, f, 0x1.c6b08ep-5f);
+    p = __fmaf_rn(p, f, 0x1.ebfbe0p-3f);
+    p = __fmaf_rn(p, f, 0x1.62e430p-1f);
+    p = __fmaf_rn(p, f, 1.0f);
+    return p;
+}
+
+__device__ __forceinline__ uint32_t fx_weight(float y, float m) {
+    float t = __fmul_rn(__fsub_rn(y, m), 0x1.715476p+0f);
+    if (!(t >= -24.0f)) return 0u;
+    float n = rintf(t);
+    float f = __fsub_rn(t, n);
+    float scale = __uint_as_float((uint32_t)(127 + 24 + (int)n) << 23);   // 2^(24+n), exact
+    return __float2uint_rd(__fmul_rn(fx_exp2_poly(f), scale));
+}
+
+// floor(n / d) for n < 2^70, d >= 1, quotient < 2^26: double estimate, then one exact correction step.
+__device__ __forceinline__ u64 udiv_small_quotient(u128 n, u64 d) {
+    double qd = (double)n / (double)d;
+    u64 q = (u64)qd;
+    u128 prod = (u128)q * d;
+    if (prod > n) --q;
+    else if (prod + d <= n) ++q;
+    return q;
+}
+
+template <int LDT> struct Logit;
+template <> struct Logit<SV_F32> {
+    using T = float;
+    static constexpr int kVec = 4;
+    __device__ static void load_vec(const T* p, float* z) {
+        float4 v = __ldg(reinterpret_cast<const float4*>(p));
+        z[0] = v.x; z[1] = v.y; z[2] = v.z; z[3] = v.w;
+    }
+    __device__ static float load(const T* p) { return __ldg(p); }
+};
+template <> struct Logit<SV_BF16> {
+    using T = uint16_t;
+    static constexpr int kVec = 8;
+    __device__ static void load_vec(const T* p, float* z) {
+        uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            z[2 * i] = __uint_as_float(w[i] << 16);
+            z[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+    __device__ static float load(const T* p) { return bf16_bits_to_float(__ldg(p)); }
+};
+
+// ------------------------------------------------------------------------------------ kernel 1: rows
+struct RowPart {
+    float zmax;
+    int zarg;
+    float ymax;
+    int fin;
+    u64 S;
+};
+
+__device__ __forceinline__ void argmax_combine(float& v, int& i, float v2, int i2) {
+    if (v2 > v || (v2 == v && i2 < i)) { v = v2; i = i2; }
+}
+
+template <int LDT, bool STOCH>
+__global__ void __launch_bounds__(kRowThreads) accept_rows_kernel(AcceptArgs a, int CL, int chunk, int rows_src) {
+    using LG = Logit<LDT>;
+    using LT = typename LG::T;
+    constexpr int VEC = LG::kVec;
+    cg::cluster_group cluster = cg::this_cluster();
+    __shared__ RowPart s_warp[kRowThreads / 32];
+    __shared__ RowPart s_part;   // this CTA's partial, read by the whole cluster
+
+    const int rank = (int)cluster.block_rank();
+    const int row = blockIdx.x / CL;
+    const bool is_draft = row >= rows_src;
+    const int r = is_draft ? row - rows_src : row;
+    const int V = a.V;
+    const LT* base = (const LT*)(is_draft ? a.draft : a.target) + (size_t)r * V;
+    const int c0 = min(V, rank * chunk), c1 = min(V, c0 + chunk);
+    const float invT = a.invT;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    float zmax = -INFINITY, ymax = -INFINITY;
+    int zarg = 0x7fffffff;
+    int zfin = 1, yfin = 1;
+    auto visit = [&](float z, int k) {
+        zfin &= isfinite(z) ? 1 : 0;
+        if (z > zmax) { zmax = z; zarg = k; }
+        if (STOCH) {
+            float y = __fmul_rn(z, invT);
+            yfin &= isfinite(y) ? 1 : 0;
+            ymax = fmaxf(ymax, y);
+        }
+    };
+    const bool vec_ok = (V % VEC) == 0;   // every row 16-byte aligned (base checked on the host)
+    if (vec_ok) {
+        for (int k = c0 + tid * VEC; k < c1; k += kRowThreads * VEC) {
+            float z[VEC];
+            LG::load_vec(base + k, z);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) visit(z[e], k + e);
+        }
+    } else {
+        for (int k = c0 + tid; k < c1; k += kRowThreads) visit(LG::load(base + k), k);
+    }
+    // block combine
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        float v2 = __shfl_xor_sync(0xffffffffu, zmax, o);
+        int i2 = __shfl_xor_sync(0xffffffffu, zarg, o);
+        argmax_combine(zmax, zarg, v2, i2);
+        ymax = fmaxf(ymax, __shfl_xor_sync(0xffffffffu, ymax, o));
+    }
+    zfin = __all_sync(0xffffffffu, zfin);
+    yfin = __all_sync(0xffffffffu, yfin);
+    if (lane == 0) s_warp[warp] = RowPart{zmax, zarg, ymax, zfin & yfin, 0};
+    __syncthreads();
+    if (tid == 0) {
+        RowPart p = s_warp[0];
+        for (int w = 1; w < kRowThreads / 32; ++w) {
+            argmax_combine(p.zmax, p.zarg, s_warp[w].zmax, s_warp[w].zarg);
+            p.ymax = fmaxf(p.ymax, s_warp[w].ymax);
+            p.fin &= s_warp[w].fin;
+        }
+        s_part = p;
+    }
+    // z-finiteness of this CTA (for the argmax output)
+    __shared__ int s_zfin;
+    int zfin_blk = __syncthreads_and(zfin);
+    if (tid == 0) s_zfin = zfin_blk;
+    cluster.sync();
+    // cluster combine: every CTA reads every partial, so all agree on the row maximum
+    RowPart tot = *cluster.map_shared_rank(&s_part, 0);
+    int zfin_all = *cluster.map_shared_rank(&s_zfin, 0);
+    for (int q = 1; q < CL; ++q) {
+        RowPart p = *cluster.map_shared_rank(&s_part, q);
+        argmax_combine(tot.zmax, tot.zarg, p.zmax, p.zarg);
+        tot.ymax = fmaxf(tot.ymax, p.ymax);
+        tot.fin &= p.fin;
+        zfin_all &= *cluster.map_shared_rank(&s_zfin, q);
+    }
+    cluster.sync();   // partials consumed; s_part may be reused
+
+    u64 S = 0;
+    if (STOCH && tot.fin) {
+        const float m = tot.ymax;
+        if (vec_ok) {
+            for (int k = c0 + tid * VEC; k < c1; k += kRowThreads * VEC) {
+                float z[VEC];
+                LG::load_vec(base + k, z);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) S += fx_weight(__fmul_rn(z[e], invT), m);
+            }
+        } else {
+            for (int k = c0 + tid; k < c1; k += kRowThreads) S += fx_weight(__fmul_rn(LG::load(base + k), invT), m);
+        }
+    }
+    if (STOCH) {
+        S = warp_sum_u64(S);
+        __shared__ u64 s_ws[kRowThreads / 32];
+        if (lane == 0) s_ws[warp] = S;
+        __syncthreads();
+        if (tid == 0) {
+            u64 t = 0;
+            for (int w = 0; w < kRowThreads / 32; ++w) t += s_ws[w];
+            s_part.S = t;
+        }
+        cluster.sync();
+        if (rank == 0 && tid == 0) {
+            u64 t = 0;
+            for (int q = 0; q < CL; ++q) t += cluster.map_shared_rank(&s_part, q)->S;
+            tot.S = t;
+        }
+        cluster.sync();
+    }
+    if (rank == 0 && tid == 0) {
+        RowStat st;
+        st.zmax = tot.zmax;
+        st.arg = zfin_all ? tot.zarg : -1;
+        st.ymax = tot.ymax;
+        st.fin = STOCH ? tot.fin : zfin_all;
+        st.S = STOCH ? tot.S : 0;
+        ((RowStat*)a.ws)[row] = st;
+        if (a.argmax && !is_draft) a.argmax[r] = st.arg;
+    }
+    pdl_launch_dependents();
+}
+
+// ------------------------------------------------------------------------------------ kernel 2: walk
+enum { MODE_GREEDY = 0, MODE_PROB = 1, MODE_ONEHOT = 2 };
+
+struct WalkShared {
+    int32_t par[SV_MAX_T];
+    int32_t tok[SV_MAX_T];
+    int32_t path[SV_MAX_T];
+    u64 hist[SV_MAX_T];       // PROB: residual sum before each rejection; ONEHOT: rejected tokens
+    u64 red[kWalkThreads / 32];
+    u64 cta_sum;              // this CTA's share of a cluster-wide sum (read remotely)
+    int32_t found;            // sampled index found in this CTA (-1 if not)
+    int st;
+};
+
+template <int LDT, int MODE>
+__global__ void __launch_bounds__(kWalkThreads) accept_walk_kernel(AcceptArgs a, int CLW) {
+    using LG = Logit<LDT>;
+    using LT = typename LG::T;
+    cg::cluster_group cluster = cg::this_cluster();
+    __shared__ WalkShared sh;
+    const int rank = (int)cluster.block_rank();
+    const int b = blockIdx.x / CLW;
+    const int T = a.T, V = a.V, B = a.B;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float invT = a.invT;
+
+    for (int i = tid; i < T; i += kWalkThreads) {
+        sh.par[i] = a.parent[(size_t)b * T + i];
+        sh.tok[i] = a.tokens[(size_t)b * T + i];
+    }
+    pdl_wait_prior();   // row statistics of kernel 1 are visible from here on
+    __syncthreads();
+    const RowStat* stats = (const RowStat*)a.ws;
+    int st = block_tree_check(sh.par, T);
+    int bad = 0;
+    for (int c = 1 + tid; c < T; c += kWalkThreads) bad |= (sh.tok[c] < 0 || sh.tok[c] >= V);
+    if (__syncthreads_or(bad) && st == SV_OK) st = SV_ERR_INVALID_ARG;
+    if (st == SV_OK) {
+        int nf = 0;
+        for (int r = tid; r < T; r += kWalkThreads) {
+            nf |= !stats[(size_t)b * T + r].fin;
+            if (MODE == MODE_PROB) nf |= !stats[(size_t)B * T + (size_t)b * T + r].fin;
+        }
+        if (__syncthreads_or(nf)) st = SV_ERR_NONFINITE;
+    }
+    const bool writer = rank == 0 && tid == 0;
+    if (st != SV_OK) {
+        if (rank == 0) {
+            for (int j = tid; j < T; j += kWalkThreads) {
+                a.path[(size_t)b * T + j] = -1;
+                a.out_tokens[(size_t)b * T + j] = -1;
+            }
+            if (tid == 0) {
+                a.accept_len[b] = -1;
+                a.bonus[b] = -1;
+                if (a.status) a.status[b] = st;
+            }
+        }
+        return;
+    }
+
+    int n = 0, cur = 0, bonus = -1;
+    if (MODE == MODE_GREEDY) {
+        if (writer) {
+            for (;;) {
+                int am = stats[(size_t)b * T + cur].arg;
+                int next = -1;
+                for (int c = cur + 1; c < T; ++c)
+                    if (sh.par[c] == cur && sh.tok[c] == am) { next = c; break; }
+                if (next < 0) { bonus = am; break; }
+                sh.path[n++] = next;
+                cur = next;
+            }
+            sh.st = n;
+            sh.found = bonus;
+        }
+        __syncthreads();
+        n = sh.st;
+        bonus = sh.found;
+    } else {
+        // every thread of the cluster follows the same walk on identical scalars
+        const LT* P = (const LT*)a.target;
+        const LT* Q = (const LT*)a.draft;
+        const uint32_t* U = a.uniforms + (size_t)b * T;
+        for (;;) {
+            const size_t prow = (size_t)b * T + cur;
+            const RowStat sp = stats[prow];
+            RowStat sq;
+            u64 Sq = 1;
+            if (MODE == MODE_PROB) {
+                sq = stats[(size_t)B * T + prow];
+                Sq = sq.S;
+            }
+            const LT* prow_p = P + prow * V;
+            const LT* prow_q = (MODE == MODE_PROB) ? Q + prow * V : nullptr;
+            int nrej = 0;
+            u64 Sres = sp.S;
+            // residual weight of token k after the rejections so far
+            auto wres = [&](int k) -> u64 {
+                u64 w = fx_weight(__fmul_rn(LG::load(prow_p + k), invT), sp.ymax);
+                if (MODE == MODE_ONEHOT) {
+                    for (int i = 0; i < nrej; ++i) if ((int)sh.hist[i] == k) w = 0;
+                } else if (MODE == MODE_PROB) {
+                    if (nrej) {
+                        u64 wq = fx_weight(__fmul_rn(LG::load(prow_q + k), invT), sq.ymax);
+                        for (int i = 0; i < nrej; ++i) {
+                            u128 x = (u128)w * Sq, s = (u128)wq * sh.hist[i];
+                            w = x > s ? udiv_small_quotient(x - s, Sq) : 0;
+                        }
+                    }
+                }
+                return w;
+            };
+            int next = -1, has_child = 0;
+            for (int c = cur + 1; c < T; ++c) {
+                if (sh.par[c] != cur) continue;
+                has_child = 1;
+                const int x = sh.tok[c];
+                const u64 wpx = wres(x);
+                const u64 wqx = (MODE == MODE_PROB) ? fx_weight(__fmul_rn(LG::load(prow_q + x), invT), sq.ymax) : 1u;
+                if ((u128)U[c] * wqx * Sres < (((u128)wpx * Sq) << 32)) { next = c; break; }
+                if (MODE == MODE_ONEHOT) {
+                    sh.hist[nrej] = (u64)x;   // identical value written by every thread
+                    ++nrej;
+                    Sres -= wpx;
+                } else {
+                    if (tid == 0) sh.hist[nrej] = Sres;
+                    __syncthreads();
+                    ++nrej;
+                    Sres = 0;  // recomputed below
+                    {
+                        const int per = (V + CLW - 1) / CLW;
+                        const int k0 = min(V, rank * per), k1 = min(V, k0 + per);
+                        u64 s = 0;
+                        for (int k = k0 + tid; k < k1; k += kWalkThreads) s += wres(k);
+                        s = warp_sum_u64(s);
+                        if (lane == 0) sh.red[warp] = s;
+                        __syncthreads();
+                        if (tid == 0) {
+                            u64 t = 0;
+                            for (int w = 0; w < kWalkThreads / 32; ++w) t += sh.red[w];
+                            sh.cta_sum = t;
+                        }
+                        cluster.sync();
+                        for (int q = 0; q < CLW; ++q) Sres += *cluster.map_shared_rank(&sh.cta_sum, q);
+                        cluster.sync();
+                    }
+                }
+            }
+            if (next >= 0) {
+                if (tid == 0) sh.path[n] = next;
+                ++n;
+                cur = next;
+                __syncthreads();
+                continue;
+            }
+            // the walk stops at `cur`: draw the bonus token from the residual (or the row itself)
+            const bool use_res = has_child && Sres != 0;
+            const u64 R = use_res ? Sres : sp.S;
+            if (!use_res) nrej = 0;
+            const u128 thr = ((u128)U[0] * R) >> 32;
+            const int per = (V + CLW - 1) / CLW;
+            const int k0 = min(V, rank * per), k1 = min(V, k0 + per);
+            // per-warp contiguous segments of this CTA's slice
+            const int nw = kWalkThreads / 32;
+            const int seg = (k1 - k0 + nw - 1) / nw;
+            const int s0 = min(k1, k0 + warp * seg), s1 = min(k1, s0 + seg);
+            u64 ws = 0;
+            for (int k = s0 + lane; k < s1; k += 32) ws += wres(k);
+            ws = warp_sum_u64(ws);
+            if (lane == 0) sh.red[warp] = ws;
+            __syncthreads();
+            if (tid == 0) {
+                u64 t = 0;
+                for (int w = 0; w < nw; ++w) t += sh.red[w];
+                sh.cta_sum = t;
+                sh.found = -1;
+            }
+            cluster.sync();
+            u64 before = 0;   // weight mass of the CTAs before this one
+            for (int q = 0; q < rank; ++q) before += *cluster.map_shared_rank(&sh.cta_sum, q);
+            if (thr >= before && thr < before + sh.cta_sum) {
+                // this CTA holds the draw: find the warp, then the element
+                u64 wb = before;
+                int wsel = -1;
+                for (int w = 0; w < nw; ++w) {
+                    if (thr < wb + sh.red[w]) { wsel = w; break; }
+                    wb += sh.red[w];
+                }
+                if (warp == wsel) {
+                    u64 run = wb;
+                    for (int k = s0; k < s1; k += 32) {
+                        u64 w = (k + lane < s1) ? wres(k + lane) : 0;
+                        u64 incl = w;
+#pragma unroll
+                        for (int o = 1; o < 32; o <<= 1) {
+                            u64 v = __shfl_up_sync(0xffffffffu, incl, o);
+                            if (lane >= o) incl += v;
+                        }
+                        unsigned hit = __ballot_sync(0xffffffffu, (u128)run + incl > thr && k + lane < s1);
+                        if (hit) {
+                            if (lane == 0) sh.found = k + __ffs(hit) - 1;
+                            break;
+                        }
+                        run += __shfl_sync(0xffffffffu, incl, 31);
+                    }
+                }
+            }
+            cluster.sync();
+            int f = -1;
+            for (int q = 0; q < CLW && f < 0; ++q) f = *cluster.map_shared_rank(&sh.found, q);
+            cluster.sync();
+            bonus = f < 0 ? V - 1 : f;
+            break;
+        }
+        __syncthreads();
+    }
+    if (rank == 0) {
+        for (int j = tid; j < T; j += kWalkThreads) {
+            a.path[(size_t)b * T + j] = j < n ? sh.path[j] : -1;
+            a.out_tokens[(size_t)b * T + j] = j < n ? sh.tok[sh.path[j]] : (j == n ? bonus : -1);
+        }
+        if (tid == 0) {
+            a.accept_len[b] = n;
+            a.bonus[b] = bonus;
+            if (a.status) a.status[b] = SV_OK;
+        }
+    }
+}
+
+int pick_cluster(int V, int per_cta) {
+    int c = (V + per_cta - 1) / per_cta;
+    return c < 1 ? 1 : (c > kMaxCluster ? kMaxCluster : c);
+}
+
+template <int LDT>
+cudaError_t launch_typed(const AcceptArgs& a, cudaStream_t s) {
+    constexpr int VEC = Logit<LDT>::kVec;
+    const bool stoch = a.temperature > 0.f;
+    const int mode = !stoch ? MODE_GREEDY : (a.draft ? MODE_PROB : MODE_ONEHOT);
+    const int rows_src = a.B * a.T;
+    const int rows = rows_src * (mode == MODE_PROB ? 2 : 1);
+    const int CL = pick_cluster(a.V, kRowThreads * VEC * 4);
+    int chunk = (a.V + CL - 1) / CL;
+    chunk = (chunk + VEC - 1) / VEC * VEC;
+    cudaError_t e;
+    if (stoch) e = launch_ex(accept_rows_kernel<LDT, true>, dim3(CL * rows), dim3(kRowThreads), 0, s, CL, false, a, CL, chunk, rows_src);
+    else       e = launch_ex(accept_rows_kernel<LDT, false>, dim3(CL * rows), dim3(kRowThreads), 0, s, CL, false, a, CL, chunk, rows_src);
+    if (e != cudaSuccess) return e;
+    const int CLW = (mode == MODE_GREEDY) ? 1 : pick_cluster(a.V, kWalkThreads * 8);
+    switch (mode) {
+    case MODE_GREEDY: return launch_ex(accept_walk_kernel<LDT, MODE_GREEDY>, dim3(a.B), dim3(kWalkThreads), 0, s, 1, true, a, 1);
+    case MODE_PROB:   return launch_ex(accept_walk_kernel<LDT, MODE_PROB>, dim3(a.B * CLW), dim3(kWalkThreads), 0, s, CLW, true, a, CLW);
+    default:          return launch_ex(accept_walk_kernel<LDT, MODE_ONEHOT>, dim3(a.B * CLW), dim3(kWalkThreads), 0, s, CLW, true, a, CLW);
+    }
+}
+
+}  // namespace
+
+size_t accept_workspace_size(int B, int T, int V) {
+    (void)V;
+    size_t rows = (size_t)2 * B * T;
+    return (rows * sizeof(RowStat) + 255) / 256 * 256;
+}
+
+cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s) {
+    if (a.B == 0) return cudaSuccess;
+    return a.logit_dt == SV_F32 ? launch_typed<SV_F32>(a, s) : launch_typed<SV_BF16>(a, s);
+}
+
+}  // namespace sv

@@ -1,0 +1,150 @@
+// attn_simt.cu -- tree-masked GQA attention on CUDA cores (fp32 arithmetic), any supported dtype.
+//
+// Serves shapes outside the tensor-core kernel's envelope (float32 inputs, D other than 64/128, small
+// problems) and is the fp32 cross-check of that kernel.  One CTA per (tree node, kv head, request) runs
+// the G query heads of the group together over the node's allowed positions: the prefix [0, L) and the
+// cache slots L + a of the node's ancestors a ("Aurora" post, section 2: the tree-attention mask follows
+// the speculative tree's causal structure).  Online softmax in the log2 domain, 32 positions per step.
+#include "sv_internal.cuh"
+
+namespace sv {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kTile = 32;
+
+template <int QDT, int KVDT>
+__global__ void __launch_bounds__(kThreads) attn_simt_kernel(AttnArgs a, float scale_log2) {
+    using QE = Elem<QDT>;
+    using KE = Elem<KVDT>;
+    extern __shared__ float smem[];
+    const int G = a.Hq / a.Hkv, D = a.D;
+    const int t = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    float* qs = smem;                       // [G][D]
+    float* os = qs + G * D;                 // [G][D]
+    float* ks = os + G * D;                 // [kTile][D+1]
+    float* vs = ks + kTile * (D + 1);       // [kTile][D]
+    float* ms = vs + kTile * D;             // [G]
+    float* ls = ms + G;                     // [G]
+    __shared__ int32_t s_par[SV_MAX_T];
+    __shared__ int32_t s_anc[SV_MAX_T];
+    __shared__ int s_nanc;
+
+    const int T = a.T;
+    for (int i = tid; i < T; i += kThreads) s_par[i] = a.parent[(size_t)b * T + i];
+    __syncthreads();
+    const int L = a.kv_len[b];
+    int st = block_tree_check(s_par, T);
+    if (st == SV_OK && (L < 0 || L + T > a.kv_cap)) st = SV_ERR_INVALID_ARG;
+
+    const size_t out_row0 = ((size_t)b * T + t) * a.Hq + (size_t)hk * G;
+    if (st != SV_OK) {
+        for (int i = tid; i < G * D; i += kThreads) {
+            if (QDT == SV_F32) ((float*)a.out)[out_row0 * D + i] = 0.f;
+            else ((uint16_t*)a.out)[out_row0 * D + i] = 0;
+        }
+        if (a.lse) for (int g = tid; g < G; g += kThreads) a.lse[out_row0 + g] = 0.f;
+        if (a.status && t == 0 && hk == 0 && tid == 0) a.status[b] = st;
+        return;
+    }
+    if (a.status && t == 0 && hk == 0 && tid == 0) a.status[b] = SV_OK;
+
+    if (tid == 0) {   // ancestors of node t (itself and the root included), as cache positions
+        int n = 0;
+        for (int x = t; x >= 0; x = s_par[x]) s_anc[n++] = L + x;
+        s_nanc = n;
+    }
+    const typename QE::T* q = (const typename QE::T*)a.q;
+    for (int i = tid; i < G * D; i += kThreads) {
+        qs[i] = QE::get(q, out_row0 * D + i);
+        os[i] = 0.f;
+    }
+    for (int g = tid; g < G; g += kThreads) { ms[g] = -INFINITY; ls[g] = 0.f; }
+    __syncthreads();
+
+    const float ksc = (KVDT == SV_E4M3) ? a.k_scale[hk] : 1.f;
+    const float vsc = (KVDT == SV_E4M3) ? a.v_scale[hk] : 1.f;
+    const typename KE::T* kp = (const typename KE::T*)a.k + ((size_t)b * a.Hkv + hk) * (size_t)a.kv_cap * D;
+    const typename KE::T* vp = (const typename KE::T*)a.v + ((size_t)b * a.Hkv + hk) * (size_t)a.kv_cap * D;
+    const int npos = L + s_nanc;
+
+    for (int start = 0; start < npos; start += kTile) {
+        for (int i = tid; i < kTile * D; i += kThreads) {
+            int r = i / D, d = i - r * D;
+            int j = start + r;
+            float kv = 0.f, vv = 0.f;
+            if (j < npos) {
+                size_t pos = (size_t)(j < L ? j : s_anc[j - L]);
+                kv = KE::get(kp, pos * D + d) * ksc;
+                vv = KE::get(vp, pos * D + d) * vsc;
+            }
+            ks[r * (D + 1) + d] = kv;
+            vs[r * D + d] = vv;
+        }
+        __syncthreads();
+        for (int g = warp; g < G; g += kThreads / 32) {
+            float s = -INFINITY;
+            if (start + lane < npos) {
+                float acc = 0.f;
+                const float* qr = qs + g * D;
+                const float* kr = ks + lane * (D + 1);
+                for (int d = 0; d < D; ++d) acc = fmaf(qr[d], kr[d], acc);
+                s = acc * scale_log2;
+            }
+            float m_old = ms[g];
+            float m_new = fmaxf(m_old, warp_max(s));
+            float p = (s == -INFINITY) ? 0.f : exp2f(s - m_new);
+            float alpha = (m_old == -INFINITY) ? 0.f : exp2f(m_old - m_new);
+            float psum = warp_sum(p);
+            for (int d = lane; d < D; d += 32) {
+                float acc = os[g * D + d] * alpha;
+                for (int j = 0; j < kTile; ++j) acc = fmaf(__shfl_sync(0xffffffffu, p, j), vs[j * D + d], acc);
+                os[g * D + d] = acc;
+            }
+            __syncwarp();
+            if (lane == 0) { ls[g] = ls[g] * alpha + psum; ms[g] = m_new; }
+            __syncwarp();
+        }
+        __syncthreads();
+    }
+
+    for (int i = tid; i < G * D; i += kThreads) {
+        int g = i / D;
+        float o = os[i] / ls[g];
+        if (QDT == SV_F32) ((float*)a.out)[out_row0 * D + i] = o;
+        else ((uint16_t*)a.out)[out_row0 * D + i] = float_to_bf16_bits(o);
+    }
+    if (a.lse)
+        for (int g = tid; g < G; g += kThreads) a.lse[out_row0 + g] = (ms[g] + log2f(ls[g])) * 0.69314718055994531f;
+}
+
+template <int QDT, int KVDT>
+cudaError_t launch_typed(const AttnArgs& a, cudaStream_t s) {
+    const int G = a.Hq / a.Hkv;
+    size_t smem = sizeof(float) * ((size_t)2 * G * a.D + (size_t)kTile * (a.D + 1) + (size_t)kTile * a.D + 2 * G);
+    auto kern = attn_simt_kernel<QDT, KVDT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    float scale = a.sm_scale != 0.f ? a.sm_scale : (float)(1.0 / sqrt((double)a.D));
+    dim3 grid(a.T, a.Hkv, a.B);
+    kern<<<grid, kThreads, smem, s>>>(a, scale * 1.4426950408889634f);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t s) {
+    if (a.B == 0) return cudaSuccess;
+    if (a.q_dt == SV_F32) {
+        if (a.kv_dt == SV_F32) return launch_typed<SV_F32, SV_F32>(a, s);
+        if (a.kv_dt == SV_BF16) return launch_typed<SV_F32, SV_BF16>(a, s);
+        return launch_typed<SV_F32, SV_E4M3>(a, s);
+    }
+    if (a.kv_dt == SV_F32) return launch_typed<SV_BF16, SV_F32>(a, s);
+    if (a.kv_dt == SV_BF16) return launch_typed<SV_BF16, SV_BF16>(a, s);
+    return launch_typed<SV_BF16, SV_E4M3>(a, s);
+}
+
+}  // namespace sv

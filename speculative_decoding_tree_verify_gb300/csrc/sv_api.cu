@@ -1,0 +1,119 @@
+// sv_api.cu -- the C ABI of libsv.so: synchronous validation of host-visible arguments, then launches.
+// Semantics, layouts and error behaviour are documented in include/sv.h.
+#include <math.h>
+
+#include "sv_internal.cuh"
+
+using namespace sv;
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+size_t dt_size(sv_dtype d) { return d == SV_F32 ? 4 : (d == SV_BF16 ? 2 : 1); }
+
+// Most of the work is asynchronous; a failed launch surfaces here.
+sv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SV_OK : SV_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* sv_status_string(sv_status s) {
+    switch (s) {
+    case SV_OK: return "ok";
+    case SV_ERR_INVALID_ARG: return "invalid argument";
+    case SV_ERR_BAD_TREE: return "parent array is not a topological tree rooted at node 0";
+    case SV_ERR_TREE_TOO_LARGE: return "tree has more than 64 nodes";
+    case SV_ERR_UNSUPPORTED: return "unsupported dtype, shape or alignment";
+    case SV_ERR_NONFINITE: return "non-finite logits";
+    case SV_ERR_TIMEOUT: return "bounded device wait timed out";
+    case SV_ERR_CUDA: return "CUDA launch failed";
+    case SV_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+int sv_version(void) { return 100; }
+
+size_t sv_workspace_size(sv_op op, int B, int T, int Hq, int Hkv, int D, int kv_cap, int V) {
+    if (B < 0 || T < 1 || T > SV_MAX_T) return 0;
+    switch (op) {
+    case SV_OP_TREE_ATTN: return attn_workspace_size(B, T, Hq, Hkv, D, kv_cap);
+    case SV_OP_ACCEPT: return accept_workspace_size(B, T, V);
+    case SV_OP_LOSS: return loss_workspace_size(B, T, V);
+    }
+    return 0;
+}
+
+sv_status sv_tree_attn(int B, int T, int Hq, int Hkv, int D, int kv_cap, sv_dtype q_dt, sv_dtype kv_dt,
+                       const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                       const float* v_scale, const int32_t* kv_len, const int32_t* parent, float sm_scale,
+                       void* out, float* lse, int32_t* status, void* workspace, size_t ws_bytes,
+                       sv_stream_t stream) {
+    if (T > SV_MAX_T) return SV_ERR_TREE_TOO_LARGE;
+    if (B < 0 || B > 65535 || T < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || D < 1 || kv_cap < T) return SV_ERR_INVALID_ARG;
+    if (!(sm_scale >= 0.f) || isinf(sm_scale)) return SV_ERR_INVALID_ARG;
+    if ((q_dt != SV_F32 && q_dt != SV_BF16) || (kv_dt != SV_F32 && kv_dt != SV_BF16 && kv_dt != SV_E4M3))
+        return SV_ERR_UNSUPPORTED;
+    if (B == 0) return SV_OK;
+    if (!q || !k_cache || !v_cache || !kv_len || !parent || !out) return SV_ERR_INVALID_ARG;
+    if (kv_dt == SV_E4M3 && (!k_scale || !v_scale)) return SV_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(kv_len, 4) || !aligned(parent, 4) || !aligned(lse, 4) || !aligned(status, 4) ||
+        !aligned(k_scale, 4) || !aligned(v_scale, 4))
+        return SV_ERR_UNSUPPORTED;
+    AttnArgs a{B, T, Hq, Hkv, D, kv_cap, q_dt, kv_dt, q, k_cache, v_cache, k_scale, v_scale, kv_len, parent,
+               sm_scale, out, lse, status, workspace, ws_bytes};
+    const bool tc = attn_tc_supported(a);
+    if (!tc && (D > 256 || (size_t)(Hq / Hkv) * D > 4096)) return SV_ERR_UNSUPPORTED;
+    const size_t need = tc ? attn_workspace_size(B, T, Hq, Hkv, D, kv_cap) : 0;
+    if (need && (!workspace || ws_bytes < need || !aligned(workspace, 256))) return SV_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    return from_cuda(tc ? launch_attn_tc(a, s) : launch_attn_simt(a, s));
+}
+
+sv_status sv_accept(int B, int T, int V, sv_dtype logit_dt, const void* target_logits,
+                    const void* draft_logits, const int32_t* tokens, const int32_t* parent, float temperature,
+                    const uint32_t* uniforms, int32_t* accept_len, int32_t* path, int32_t* out_tokens,
+                    int32_t* bonus, int32_t* argmax, int32_t* status, void* workspace, size_t ws_bytes,
+                    sv_stream_t stream) {
+    if (T > SV_MAX_T) return SV_ERR_TREE_TOO_LARGE;
+    if (B < 0 || T < 1 || V < 1) return SV_ERR_INVALID_ARG;
+    if ((long long)B * T * 2 * 8 > 0x7fffffffLL) return SV_ERR_INVALID_ARG;
+    if (!(temperature >= 0.f) || isinf(temperature)) return SV_ERR_INVALID_ARG;
+    if (logit_dt != SV_F32 && logit_dt != SV_BF16) return SV_ERR_UNSUPPORTED;
+    const bool stoch = temperature > 0.f;
+    if (stoch && !uniforms) return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!target_logits || !tokens || !parent || !accept_len || !path || !out_tokens || !bonus)
+        return SV_ERR_INVALID_ARG;
+    if (!aligned(target_logits, 16) || !aligned(draft_logits, 16) || !aligned(tokens, 4) || !aligned(parent, 4) ||
+        !aligned(uniforms, 4) || !aligned(accept_len, 4) || !aligned(path, 4) || !aligned(out_tokens, 4) ||
+        !aligned(bonus, 4) || !aligned(argmax, 4) || !aligned(status, 4))
+        return SV_ERR_UNSUPPORTED;
+    const size_t need = accept_workspace_size(B, T, V);
+    if (!workspace || ws_bytes < need || !aligned(workspace, 256)) return SV_ERR_WORKSPACE;
+    AcceptArgs a{B, T, V, logit_dt, target_logits, stoch ? draft_logits : nullptr, tokens, parent, temperature,
+                 stoch ? (float)(1.0 / (double)temperature) : 1.f, uniforms, accept_len, path, out_tokens,
+                 bonus, argmax, status, workspace};
+    return from_cuda(launch_accept(a, (cudaStream_t)stream));
+}
+
+sv_status sv_loss(int N, int T, int V, const void* draft_logits, const int32_t* tokens,
+                  const int32_t* parent, const int32_t* labels, float* row_loss, float* sums, void* grad,
+                  int32_t* status, void* workspace, size_t ws_bytes, sv_stream_t stream) {
+    if (T > SV_MAX_T) return SV_ERR_TREE_TOO_LARGE;
+    if (N < 0 || T < 1 || V < 2) return SV_ERR_INVALID_ARG;
+    if ((long long)N * T * 8 > 0x7fffffffLL) return SV_ERR_INVALID_ARG;
+    if (!sums) return SV_ERR_INVALID_ARG;
+    if (N > 0 && (!draft_logits || !tokens || !parent || !labels || !row_loss)) return SV_ERR_INVALID_ARG;
+    if (!aligned(draft_logits, 16) || !aligned(grad, 16) || !aligned(tokens, 4) || !aligned(parent, 4) ||
+        !aligned(labels, 4) || !aligned(row_loss, 4) || !aligned(sums, 4) || !aligned(status, 4))
+        return SV_ERR_UNSUPPORTED;
+    const size_t need = loss_workspace_size(N, T, V);
+    if (!workspace || ws_bytes < need || !aligned(workspace, 256)) return SV_ERR_WORKSPACE;
+    LossArgs a{N, T, V, draft_logits, tokens, parent, labels, row_loss, sums, grad, status, workspace};
+    return from_cuda(launch_loss(a, (cudaStream_t)stream));
+}
+
+}  // extern "C"

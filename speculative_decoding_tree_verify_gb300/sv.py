@@ -1,0 +1,134 @@
+"""Thin Python binding of libsv.so (include/sv.h): argument marshalling only.
+
+Every function takes torch tensors that already live on the GPU, passes their device pointers, sizes and
+the current CUDA stream to the C entry point of the same name, and raises SVError on a non-OK status.  No
+computation happens here, and there is no CPU fallback: if the CUDA library has not been built, loading
+fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from pathlib import Path
+
+import torch
+
+LIB_PATH = Path(__file__).resolve().parent / "_build" / "libsv.so"
+
+OK, ERR_INVALID_ARG, ERR_BAD_TREE, ERR_TREE_TOO_LARGE, ERR_UNSUPPORTED, ERR_NONFINITE, ERR_TIMEOUT, ERR_CUDA, \
+    ERR_WORKSPACE = range(9)
+F32, BF16, E4M3 = 0, 1, 2
+OP_TREE_ATTN, OP_ACCEPT, OP_LOSS = 0, 1, 2
+
+_lib = None
+
+
+class SVError(RuntimeError):
+    def __init__(self, code: int, fn: str):
+        self.code = code
+        super().__init__(f"{fn}: {status_string(code)} (status {code})")
+
+
+def lib() -> C.CDLL:
+    global _lib
+    if _lib is None:
+        if not LIB_PATH.exists():
+            raise RuntimeError(f"libsv.so is not built ({LIB_PATH}); run "
+                               "`python -m speculative_decoding_tree_verify_gb300.build`")
+        L = C.CDLL(str(LIB_PATH))
+        P, i, f, z = C.c_void_p, C.c_int, C.c_float, C.c_size_t
+        L.sv_status_string.argtypes = [i]
+        L.sv_status_string.restype = C.c_char_p
+        L.sv_version.restype = i
+        L.sv_workspace_size.argtypes = [i] * 8
+        L.sv_workspace_size.restype = z
+        L.sv_tree_attn.argtypes = [i, i, i, i, i, i, i, i, P, P, P, P, P, P, P, f, P, P, P, P, z, P]
+        L.sv_tree_attn.restype = i
+        L.sv_accept.argtypes = [i, i, i, i, P, P, P, P, f, P, P, P, P, P, P, P, P, z, P]
+        L.sv_accept.restype = i
+        L.sv_loss.argtypes = [i, i, i, P, P, P, P, P, P, P, P, P, z, P]
+        L.sv_loss.restype = i
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().sv_status_string(int(code)).decode()
+
+
+def workspace_size(op: int, B: int, T: int, Hq: int = 0, Hkv: int = 0, D: int = 0, kv_cap: int = 0,
+                   V: int = 0) -> int:
+    return int(lib().sv_workspace_size(op, B, T, Hq, Hkv, D, kv_cap, V))
+
+
+def dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype in (torch.bfloat16, torch.uint16, torch.int16):      # bf16 values or their bit patterns
+        return BF16
+    if t.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
+        return E4M3
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to libsv must be CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libsv must be contiguous")
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return C.c_void_p(s.cuda_stream)
+
+
+def _ws(op, workspace, *dims):
+    if workspace is not None:
+        return workspace
+    n = workspace_size(op, *dims)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device="cuda") if n else None
+
+
+def _check(code, fn):
+    if code != OK:
+        raise SVError(code, fn)
+
+
+def tree_attn(q, k_cache, v_cache, kv_len, parent, out, *, k_scale=None, v_scale=None, sm_scale=0.0, lse=None,
+              status=None, workspace=None, stream=None):
+    """sv_tree_attn: q [B,T,Hq,D]; caches [B,Hkv,kv_cap,D]; out like q."""
+    B, T, Hq, D = q.shape
+    Hkv, kv_cap = k_cache.shape[1], k_cache.shape[2]
+    ws = _ws(OP_TREE_ATTN, workspace, B, T, Hq, Hkv, D, kv_cap, 0)
+    code = lib().sv_tree_attn(B, T, Hq, Hkv, D, kv_cap, dtype_code(q), dtype_code(k_cache), _ptr(q), _ptr(k_cache),
+                              _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(kv_len), _ptr(parent),
+                              float(sm_scale), _ptr(out), _ptr(lse), _ptr(status), _ptr(ws),
+                              0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
+    _check(code, "sv_tree_attn")
+
+
+def accept(target_logits, tokens, parent, accept_len, path, out_tokens, bonus, *, draft_logits=None,
+           temperature=0.0, uniforms=None, argmax=None, status=None, workspace=None, stream=None):
+    """sv_accept: logits [B,T,V]; tokens/parent [B,T]; outputs accept_len [B], path/out_tokens [B,T], bonus [B]."""
+    B, T, V = target_logits.shape
+    ws = _ws(OP_ACCEPT, workspace, B, T, 0, 0, 0, 0, V)
+    code = lib().sv_accept(B, T, V, dtype_code(target_logits), _ptr(target_logits), _ptr(draft_logits),
+                           _ptr(tokens), _ptr(parent), float(temperature), _ptr(uniforms), _ptr(accept_len),
+                           _ptr(path), _ptr(out_tokens), _ptr(bonus), _ptr(argmax), _ptr(status), _ptr(ws),
+                           ws.numel() * ws.element_size(), _stream(stream))
+    _check(code, "sv_accept")
+
+
+def loss(draft_logits, tokens, parent, labels, row_loss, sums, *, grad=None, status=None, workspace=None,
+         stream=None):
+    """sv_loss: draft_logits [N*T,V] bf16; tokens/parent/labels [N,T]; row_loss [N*T]; sums [3]; grad like logits."""
+    N, T = parent.shape
+    V = draft_logits.shape[-1]
+    ws = _ws(OP_LOSS, workspace, N, T, 0, 0, 0, 0, V)
+    code = lib().sv_loss(N, T, V, _ptr(draft_logits), _ptr(tokens), _ptr(parent), _ptr(labels), _ptr(row_loss),
+                         _ptr(sums), _ptr(grad), _ptr(status), _ptr(ws), ws.numel() * ws.element_size(),
+                         _stream(stream))
+    _check(code, "sv_loss")

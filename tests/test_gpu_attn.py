@@ -1,0 +1,100 @@
+"""GPU parity of sv_tree_attn against the oracle (float64): element by element on small shapes that span
+several KV tiles with ragged tails, and on sampled (request, node, head) rows of the named workloads at
+full size.  Tolerances: max-abs 2e-2 for bf16 outputs, 6e-2 with FP8 E4M3 KV, 1e-4 for float32 outputs
+(fp32 arithmetic throughout)."""
+import numpy as np
+import pytest
+
+import oracle
+from speculative_decoding_tree_verify_gb300 import workloads as W
+from tests.gpu_util import run_attn
+
+pytestmark = pytest.mark.gpu
+
+
+def tol(w):
+    if w.kv_dt == "e4m3":
+        return 6e-2
+    return 2e-2 if w.q_dt == "bf16" else 1e-4
+
+
+def check_full(w, sm_scale=0.0):
+    out, lse, st = run_attn(w, sm_scale)
+    ref_o, ref_l, ref_st, _ = oracle.tree_attn_w(w, sm_scale=sm_scale)
+    np.testing.assert_array_equal(st, ref_st)
+    ok = ref_st == 0
+    err = np.abs(out[ok] - ref_o[ok]).max()
+    assert err <= tol(w), err
+    assert np.abs(lse[ok] - ref_l[ok]).max() <= (1e-3 if w.q_dt == "bf16" else 1e-5)
+    return out, st
+
+
+def check_sampled(w, n_rows=384, seed=0):
+    out, lse, st = run_attn(w)
+    rng = np.random.default_rng(seed)
+    rows = np.stack([rng.integers(0, w.B, n_rows), rng.integers(0, w.T, n_rows), rng.integers(0, w.Hq, n_rows)], 1)
+    # every node of one whole request too (all tree depths, all heads)
+    b0 = int(rng.integers(0, w.B))
+    extra = np.array([[b0, i, h] for i in range(w.T) for h in range(0, w.Hq, max(1, w.Hq // 8))])
+    rows = np.concatenate([rows, extra]).astype(np.int32)
+    ref_o, ref_l, ref_st, _ = oracle.tree_attn_w(w, rows=rows)
+    assert (st == 0).all() and (ref_st == 0).all()
+    b, i, h = rows.T
+    err = np.abs(out[b, i, h] - ref_o[b, i, h]).max()
+    assert err <= tol(w), err
+    assert np.abs(lse[b, i, h] - ref_l[b, i, h]).max() <= (1e-3 if w.q_dt == "bf16" else 1e-5)
+
+
+SMALL = [
+    # B, T, Hq, Hkv, D, L, tree, q_dt, kv_dt
+    (2, 6, 4, 1, 64, (0, 0), "chain", "f32", "f32"),
+    (3, 6, 4, 1, 64, (100, 300), "chain", "f32", "f32"),
+    (2, 13, 8, 2, 128, (1, 517), (3, 2, 2), "bf16", "bf16"),
+    (2, 60, 32, 8, 128, (120, 700), (4, 3, 2, 2, 1, 1), "bf16", "bf16"),
+    (3, 9, 16, 2, 128, (200, 333), (4, 2), "bf16", "e4m3"),
+    (1, 64, 8, 8, 64, (0, 100), (4, 3, 2, 2, 1, 1, 1), "bf16", "bf16"),
+    (2, 1, 8, 1, 128, (1, 1000), "chain", "bf16", "bf16"),
+    (2, 20, 4, 2, 64, (31, 33), "star", "f32", "bf16"),
+    (2, 7, 6, 3, 96, (50, 90), (2, 2, 1), "bf16", "bf16"),
+]
+
+
+@pytest.mark.parametrize("case", SMALL)
+def test_attn_parity_small(case):
+    B, T, Hq, Hkv, D, L, tree, qdt, kvdt = case
+    w = W.make_verify(sum(L) + T, B=B, T=T, Hq=Hq, Hkv=Hkv, D=D, L=L, V=64, q_dt=qdt, kv_dt=kvdt, tree=tree)
+    check_full(w)
+
+
+def test_attn_ignores_nan_junk_beyond_the_tree():
+    w = W.make_verify(5, B=3, T=9, Hq=8, Hkv=2, D=128, L=(60, 260), V=64, q_dt="bf16", kv_dt="bf16", tree=(3, 2),
+                      junk="nan", kv_cap=400)
+    out, _ = check_full(w)
+    assert np.isfinite(out).all()
+
+
+def test_attn_sm_scale_override():
+    w = W.make_verify(6, B=2, T=6, Hq=4, Hkv=2, D=64, L=(40, 80), V=64, q_dt="f32", kv_dt="f32", tree=(2, 2))
+    check_full(w, sm_scale=0.05)
+
+
+def test_attn_status_codes():
+    w = W.make_verify(7, B=4, T=5, Hq=4, Hkv=2, D=64, L=(10, 20), V=64, q_dt="bf16", kv_dt="bf16", tree=(2, 2))
+    w.parent = w.parent.copy()
+    w.kv_len = w.kv_len.copy()
+    w.parent[1, 4] = 4
+    w.kv_len[2] = w.kv_cap - 2
+    w.kv_len[3] = -1
+    out, lse, st = run_attn(w)
+    assert list(st) == [0, 2, 1, 1]
+    assert (out[1:] == 0).all() and (lse[1:] == 0).all()
+
+
+@pytest.mark.parametrize("name", ["tiny_chain"])
+def test_named_small_workload_full(name):
+    check_full(W.make_workload(name, seed=0))
+
+
+@pytest.mark.parametrize("name", ["llama3_8b_tree", "qwen3_8b_stochastic"])
+def test_named_workloads_full_size_sampled(name):
+    check_sampled(W.make_workload(name, seed=0))
