@@ -120,7 +120,8 @@ def tree_attn(q, k, v, kv_len, parent, *, Hq, Hkv, q_dt, kv_dt, k_scale=None, v_
     out = np.full((B, T, Hq, D), np.nan)
     lse = np.full((B, T, Hq), np.nan)
     status = np.zeros(B, np.int32)
-    r = None if rows is None else np.ascontiguousarray(rows, np.int32).reshape(-1, 3)
+    r = None if rows is None else np.unique(np.asarray(rows, np.int32).reshape(-1, 3), axis=0)
+    r = None if r is None else np.ascontiguousarray(r, np.int32)
     rc = lib().or_tree_attn(B, T, Hq, Hkv, D, kv_cap, DT[q_dt], DT[kv_dt], _p(q), _p(k), _p(v), _p(ks),
                             _p(vs), _p(kv_len), _p(parent), float(sm_scale), _p(r),
                             0 if r is None else len(r), _p(out), _p(lse), _p(status))

@@ -126,15 +126,16 @@ static void attn_row(int T, int Hq, int Hkv, int D, int kv_cap, int q_dt, int kv
         if (s[j] > m) m = s[j];
     }
     double sum = 0.0;
-    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    double* acc = (double*)calloc((size_t)D, sizeof(double));   /* private accumulator, stored once */
     for (int j = 0; j < npos; ++j) {
         if (s[j] == -INFINITY) continue;
         double w = exp(s[j] - m);
         sum += w;
-        for (int d = 0; d < D; ++d) o[d] += w * (load_elem(v, kvbase + (size_t)j * D + d, kv_dt) * vs);
+        for (int d = 0; d < D; ++d) acc[d] += w * (load_elem(v, kvbase + (size_t)j * D + d, kv_dt) * vs);
     }
-    for (int d = 0; d < D; ++d) o[d] /= sum;
+    for (int d = 0; d < D; ++d) o[d] = acc[d] / sum;
     *lse_out = m + log(sum);
+    free(acc);
     free(s);
 }
 

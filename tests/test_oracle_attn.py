@@ -182,3 +182,15 @@ def test_tree_check_and_depth():
     assert oracle.tree_check(np.array([-1, 0, 5])) == 2
     st, d = oracle.tree_depth(np.array([-1, 0, 0, 1, 3, 2]))
     assert st == 0 and list(d) == [0, 1, 1, 2, 3, 2]
+
+
+def test_duplicate_sampled_rows_are_race_free():
+    """Sampled rows may repeat (random draws); every copy must equal the full computation."""
+    w = W.make_verify(12, B=2, T=16, Hq=8, Hkv=2, D=64, L=(300, 400), V=64, q_dt="bf16", kv_dt="bf16",
+                      tree=(3, 2, 2))
+    out, lse, _, _ = oracle.tree_attn_w(w)
+    rows = np.tile(np.array([[0, 3, 1], [1, 15, 7], [1, 0, 0]], np.int32), (64, 1))
+    o2, l2, _, _ = oracle.tree_attn_w(w, rows=rows)
+    for b, i, h in rows[:3]:
+        np.testing.assert_array_equal(o2[b, i, h], out[b, i, h])
+        assert l2[b, i, h] == lse[b, i, h]
