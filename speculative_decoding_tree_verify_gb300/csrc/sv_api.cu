@@ -9,7 +9,6 @@ using namespace sv;
 namespace {
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
-size_t dt_size(sv_dtype d) { return d == SV_F32 ? 4 : (d == SV_BF16 ? 2 : 1); }
 
 // Most of the work is asynchronous; a failed launch surfaces here.
 sv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SV_OK : SV_ERR_CUDA; }
