@@ -309,12 +309,14 @@ def run_sv(args, rank, world, local_rank):
     peak, peak_kind = peaks()
     ab, cb = attn_bytes(w), accept_bytes(w)
     # the dominant kernel is the one with the larger share of the step
+    tc = w.q_dt == "bf16" and w.kv_dt == "bf16" and w.D == 128
     if t_attn >= t_acc:
-        dom, byt, t_dom, src = "tree_attn", ab, t_attn, ROOT / "speculative_decoding_tree_verify_gb300/csrc/attn_simt.cu"
+        dom, byt, t_dom = "tree_attn", ab, t_attn
+        src = ROOT / "speculative_decoding_tree_verify_gb300/csrc" / ("attn_tc.cu" if tc else "attn_simt.cu")
     else:
         dom, byt, t_dom, src = "accept", cb, t_acc, ROOT / "speculative_decoding_tree_verify_gb300/csrc/accept.cu"
     achieved = byt / (t_dom * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
+    roofline = {"bound": "hbm", "kernel": dom + (" (planner + attn_tc_kernel)" if dom == "tree_attn" and tc else ""), "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
                 "unit": "GB/s", "frac": achieved / peak, "algorithmic_bytes_per_launch": byt,
                 "traffic": traffic_from_profile(src, args.workload),
                 "step_frac": (ab + cb) / (ms * 1e-3) / 1e9 / peak}
@@ -322,7 +324,7 @@ def run_sv(args, rank, world, local_rank):
     if not args.no_cpu_baseline:
         v, cores, desc = cpu_oracle_sample(w, args.cpu_seconds)
         cpu = {"value": v, "unit": "nodes/s", "cores": cores, "kind": "oracle", "sample": desc}
-    launches_per_step = (1 if ws_attn_n == 0 else 3) + 2
+    launches_per_step = (2 if tc else 1) + 2     # [planner +] attention kernel, accept rows + walk
     line = {"metric": METRIC, "value": value, "unit": "nodes/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": w.q_dt, "data": "synthetic",

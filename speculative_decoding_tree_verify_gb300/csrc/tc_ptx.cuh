@@ -17,9 +17,12 @@
 namespace sv {
 namespace tc {
 
-// Every wait on an mbarrier gives up after this many polls (each poll may itself block for a bounded,
-// hardware-defined time), so a lost arrival ends the kernel with an error instead of hanging the GPU.
-constexpr uint32_t kSpinLimit = 1u << 22;
+// Waits on an mbarrier sleep in hardware until the phase completes (try_wait with a suspend-time hint, so a
+// waiting warp does not steal issue slots from the warps doing the work) and give up after kSpinLimit
+// tries of at most kSuspendNs each (about one second in all): a lost arrival ends the kernel with an error
+// instead of hanging the GPU.
+constexpr uint32_t kSpinLimit = 1u << 12;
+constexpr uint32_t kSuspendNs = 250000;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -38,10 +41,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
         : "memory");
     return ok != 0;
 }
@@ -49,7 +52,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* err) {
     for (uint32_t i = 0; i < kSpinLimit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 1023u) == 1023u && *err) return false;   // another role already gave up
+        if (*err) return false;   // another role already gave up
     }
     *err = 1;
     return false;
@@ -91,6 +94,17 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uin
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
         ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem]^T: A (M x 16 per instruction) is read from TMEM, two bf16 per 32-bit
+// column with the even k in the low half.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 // Arrive once on the mbarrier when every tcgen05 operation this thread issued before has completed.
