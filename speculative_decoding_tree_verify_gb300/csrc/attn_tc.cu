@@ -45,7 +45,7 @@ constexpr int kHalfBytes = kSlotBytes / 2;       // one 64-column box of a tile
 constexpr int kThreads = 384;
 constexpr int kMaxGrid = 160;                    // the workspace is sized for grids up to this size
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
-constexpr int kMergeThreads = 256;
+constexpr int kMergeThreads = 256;              // 8 warps
 
 constexpr int kSmemQ = 0;                        // [2 M tiles][2 halves][16 KB]
 constexpr int kSmemRing = 65536;                 // [10][16 KB]
@@ -57,11 +57,23 @@ constexpr int kSmemAlloc = kSmemBytes + 1024;                  // + alignment sl
 __host__ __device__ constexpr uint32_t col_S(int j, uint32_t b) { return 64u * (2u * (uint32_t)j + b); }
 __host__ __device__ constexpr uint32_t col_O(int j) { return 256u + 128u * (uint32_t)j; }
 
-// Workspace: a 256-byte header (time-out flag) and two partial-result slots per CTA.
+// Workspace: a 256-byte header (time-out flag); per CTA a record of the split pair it completes (if any);
+// two partial-result slots per CTA.
 // A slot holds O / l in bf16 [256 rows][128], then m (log2 units) [256] and l [256] in fp32.
+struct SplitRec {
+    int pair;            // -1: this CTA completes no split pair (or the request's tree is malformed)
+    int b, hk, qg;       // request, kv head and query group of the pair
+    int cf;              // first CTA holding a segment of the pair
+    int cf_slot;         // that CTA's slot for the pair (2 cf, or 2 cf + 1 if it began in an earlier pair)
+    int pad[2];
+};
 __host__ __device__ constexpr long long slot_bytes() { return (long long)kGroupRows * kD * 2 + kGroupRows * 8; }
-__host__ __device__ constexpr long long slots_off() { return 256; }
-__host__ __device__ constexpr long long workspace_bytes() { return slots_off() + 2LL * kMaxGrid * slot_bytes(); }
+__host__ __device__ constexpr long long rec_off() { return 256; }
+__host__ __device__ inline long long slots_off(int B) {
+    (void)B;
+    return (rec_off() + kMaxGrid * (long long)sizeof(SplitRec) + 255) / 256 * 256;
+}
+__host__ __device__ inline long long workspace_bytes(int B) { return slots_off(B) + 2LL * kMaxGrid * slot_bytes(); }
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -156,6 +168,7 @@ struct Seg {
     int pair, b, hk, qg, t0, t1;   // tiles [t0, t1) of the pair
     bool split;                    // the pair crosses a range boundary
     int slot;                      // partial-result slot (split segments only)
+    long long s0, s1;              // global tiles of the whole pair
 };
 
 struct SegIter {
@@ -194,6 +207,8 @@ struct SegIter {
             s.t1 = (int)(e - s0);
             s.split = !(s0 >= lo && s1 <= hi);
             s.slot = (lo >= s0 && lo < s1) ? 2 * c : 2 * c + 1;
+            s.s0 = s0;
+            s.s1 = s1;
             t = e;
             ++lp;
             return true;
@@ -375,6 +390,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         SegIter si;
         si.init(a, plan, HQ, QG);
         Seg sg;
+        bool first_seg = true;
         while (si.next(sg)) {
             const int b = sg.b, hk = sg.hk;
             const int MT = (min(kGroupRows, TG - sg.qg * kGroupRows) + 127) / 128;
@@ -387,12 +403,27 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             const bool valid_row = qi < TG;
             const int t_node = valid_row ? qi / G : 0, g_head = valid_row ? qi - (qi / G) * G : 0;
             const size_t out_row = ((size_t)b * T + t_node) * a.Hq + (size_t)hk * G + g_head;
-            uint8_t* part = sg.split ? (uint8_t*)a.ws + slots_off() + (long long)sg.slot * slot_bytes() : nullptr;
+            uint8_t* part = sg.split ? (uint8_t*)a.ws + slots_off(a.B) + (long long)sg.slot * slot_bytes() : nullptr;
             // ancestors of this row's node from the request's parent array (walk bounded by T, so a malformed
             // array cannot trap; such requests are zeroed and flagged by the merge kernel)
             wg_sync();
             if (row < T) sh.par[j][row] = __ldg(a.parent + (size_t)b * T + row);
             wg_sync();
+            if (j == 0 && row == 0 && first_seg) {
+                // the pair that began in an earlier CTA range and ends in this one is merged by attn_merge_kernel
+                int bad = sh.par[0][0] != -1;
+                for (int x = 1; x < T; ++x) bad |= sh.par[0][x] < 0 || sh.par[0][x] >= x;
+                SplitRec r;
+                r.pair = (sg.s0 < plan.lo && sg.s1 <= plan.hi && !bad) ? sg.pair : -1;
+                r.b = b;
+                r.hk = hk;
+                r.qg = sg.qg;
+                r.cf = owner_of(sg.s0, plan.total, plan.grid);
+                r.cf_slot = ((long long)r.cf * plan.total / plan.grid == sg.s0) ? 2 * r.cf : 2 * r.cf + 1;
+                r.pad[0] = r.pad[1] = 0;
+                ((SplitRec*)((uint8_t*)a.ws + rec_off()))[blockIdx.x] = r;
+            }
+            first_seg = false;
             uint64_t anc = 0;
             if (valid_row) {
                 int x = t_node;
@@ -555,6 +586,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             }
         }
     }
+    if (!active && tid == 0) {   // CTAs beyond the used grid complete no split pair
+        SplitRec r = {};
+        r.pair = -1;
+        ((SplitRec*)((uint8_t*)a.ws + rec_off()))[blockIdx.x] = r;
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -565,23 +601,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 }
 
 // ------------------------------------------------------------------------------------------------ merge kernel
-// Runs after attn_tc_kernel: validates every request (statuses, zero outputs for failed ones) and merges
-// the segments of every pair that crossed a CTA range boundary.
-__global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(AttnArgs a, int grid_launch) {
-    __shared__ long long s_warp[33];
+// Runs after attn_tc_kernel (programmatic dependent launch): validates every request (statuses, zero
+// outputs for failed ones) and merges the segments of every pair that crossed a CTA range boundary.
+// One merge unit = (record of CTA c, 16 rows): each warp merges two rows, lanes covering 4 of the 128 dims
+// (coalesced 8-byte loads), with every load of a row issued before any of them is used.
+constexpr int kMergeRows = 16;
+constexpr int kMergeUnits = kGroupRows / kMergeRows;   // per record
+
+__global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(AttnArgs a, int grid_main) {
     __shared__ int s_bad;
-    const int T = a.T, G = a.Hq / a.Hkv, TG = T * G, QG = (TG + kGroupRows - 1) / kGroupRows, HQ = a.Hkv * QG;
-    const int tid = threadIdx.x;
-    // the same global tile numbering as the attention kernel (its grid size is passed in)
-    long long sum = 0;
-    for (int b = tid; b < a.B; b += blockDim.x) sum += tiles_of(a, b);
-    long long reqs;
-    block_scan(sum, s_warp, &reqs);
-    const long long total = reqs * HQ;
-    const int grid = (long long)grid_launch < total ? grid_launch : (int)total;
+    const int T = a.T, G = a.Hq / a.Hkv, TG = T * G;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_wait_prior();   // attention results are visible from here on
     const bool timeout = *(volatile const int*)a.ws != 0;
-    auto tree_bad = [&](int b) {   // all threads call; true if request b's parent array is malformed
+
+    // 1. statuses, and zero outputs of failed requests
+    for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
         if (tid == 0) s_bad = 0;
         __syncthreads();
         if (tid < T) {
@@ -589,15 +624,8 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(AttnArgs a, i
             if (tid == 0 ? p != -1 : (p < 0 || p >= tid)) s_bad = 1;
         }
         __syncthreads();
-        const bool bad = s_bad != 0;
-        __syncthreads();
-        return bad;
-    };
-
-    // 1. statuses, and zero outputs of failed requests
-    for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
         const int L = __ldg(a.kv_len + b);
-        int st = tree_bad(b) ? SV_ERR_BAD_TREE : SV_OK;
+        int st = s_bad ? SV_ERR_BAD_TREE : SV_OK;
         if (st == SV_OK && (L < 0 || L + T > a.kv_cap)) st = SV_ERR_INVALID_ARG;
         if (timeout) st = SV_ERR_TIMEOUT;
         if (tid == 0 && a.status) a.status[b] = st;
@@ -607,85 +635,71 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(AttnArgs a, i
             for (size_t i = tid; i < n * kD / 8; i += blockDim.x) ((uint4*)o)[i] = make_uint4(0, 0, 0, 0);
             if (a.lse) for (size_t i = tid; i < n; i += blockDim.x) a.lse[(size_t)b * n + i] = 0.f;
         }
+        __syncthreads();
     }
-    if (grid <= 0 || timeout) return;
-    // 2. merges.  Request b's pairs start at req_start(b) + lp * tiles(b); walk requests in order.
-    const uint8_t* slots = (const uint8_t*)a.ws + slots_off();
-    long long req_start = 0;
-    for (int b = 0; b < a.B; ++b) {
-        const int tiles = tiles_of(a, b);
-        if (tiles == 0) continue;
-        const long long rs = req_start;
-        req_start += (long long)HQ * tiles;
-        bool checked = false, bad = false;
-        for (int lp = 0; lp < HQ; ++lp) {
-            const int pair = b * HQ + lp;
-            if (pair % (int)gridDim.x != (int)blockIdx.x) continue;
-            const long long s0 = rs + (long long)lp * tiles, s1 = s0 + tiles;
-            const int cf = owner_of(s0, total, grid), cl = owner_of(s1 - 1, total, grid);
-            if (cf == cl) continue;                       // unsplit: written directly
-            if (!checked) {                               // malformed trees were zeroed above
-                bad = tree_bad(b);
-                checked = true;
-            }
-            if (bad) continue;
-            const long long lo_cf = (long long)cf * total / grid;
-            const int hk = lp / QG, qg = lp - hk * QG;
-            const int rows = min(kGroupRows, TG - qg * kGroupRows);
-            for (int r = tid; r < rows; r += blockDim.x) {
-                const int qi = qg * kGroupRows + r, t_node = qi / G, g_head = qi - t_node * G;
-                const size_t out_row = ((size_t)b * T + t_node) * a.Hq + (size_t)hk * G + g_head;
-                // segment of CTA c: its first pair (slot 2c) unless c = cf started before this pair (2c+1)
-                auto slot_of = [&](int c) {
-                    const int s = (c > cf || lo_cf == s0) ? 2 * c : 2 * c + 1;
-                    return slots + (long long)s * slot_bytes();
-                };
-                float M = -INFINITY;
-                for (int c = cf; c <= cl; ++c)
-                    M = fmaxf(M, __ldcg((const float*)(slot_of(c) + (size_t)kGroupRows * kD * 2) + r));
-                float Lsum = 0.f;
-                for (int c = cf; c <= cl; ++c) {
-                    const float* ml = (const float*)(slot_of(c) + (size_t)kGroupRows * kD * 2);
-                    Lsum += __ldcg(ml + kGroupRows + r) * ex2(__ldcg(ml + r) - M);   // ex2(-inf) = 0
+    if (timeout) return;
+    // 2. merges
+    const SplitRec* recs = (const SplitRec*)((const uint8_t*)a.ws + rec_off());
+    const uint8_t* slots = (const uint8_t*)a.ws + slots_off(a.B);
+    for (int u = blockIdx.x; u < grid_main * kMergeUnits; u += gridDim.x) {
+        const int cl = u / kMergeUnits, rb = u - cl * kMergeUnits;
+        const SplitRec rec = recs[cl];
+        if (rec.pair < 0) continue;
+        const int rows = min(kGroupRows, TG - rec.qg * kGroupRows);
+        float m[2][4], l[2][4];
+        uint2 x[2][4];
+        int rr[2];
+        // contributors are CTAs cf..cl; CTA c > cf holds the pair in its first slot 2c
+        for (int h = 0; h < 2; ++h) rr[h] = rb * kMergeRows + warp * 2 + h;
+        float M[2] = {-INFINITY, -INFINITY}, Ls[2] = {0.f, 0.f}, acc[2][4] = {};
+        for (int c0 = rec.cf; c0 <= cl; c0 += 4) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int c = min(c0 + i, cl);
+                    const int sidx = c == rec.cf ? rec.cf_slot : 2 * c;
+                    const uint8_t* base = slots + (long long)sidx * slot_bytes();
+                    const int r = min(rr[h], rows - 1);
+                    const float* ml = (const float*)(base + (size_t)kGroupRows * kD * 2);
+                    m[h][i] = c0 + i <= cl ? __ldcg(ml + r) : -INFINITY;
+                    l[h][i] = __ldcg(ml + kGroupRows + r);
+                    x[h][i] = __ldcg((const uint2*)((const uint16_t*)base + (size_t)r * kD) + lane);
                 }
-                const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-#pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    float acc[64];
-#pragma unroll
-                    for (int e = 0; e < 64; ++e) acc[e] = 0.f;
-                    for (int c = cf; c <= cl; ++c) {
-                        const uint8_t* sp = slot_of(c);
-                        const float* ml = (const float*)(sp + (size_t)kGroupRows * kD * 2);
-                        const float wgt = __ldcg(ml + kGroupRows + r) * ex2(__ldcg(ml + r) - M) * inv;
-                        const uint4* src = (const uint4*)((const uint16_t*)sp + (size_t)r * kD + half * 64);
-                        uint4 x[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) x[e] = __ldcg(src + e);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const uint32_t w4[4] = {x[e].x, x[e].y, x[e].z, x[e].w};
-#pragma unroll
-                            for (int h = 0; h < 4; ++h) {
-                                acc[8 * e + 2 * h] += __uint_as_float(w4[h] << 16) * wgt;
-                                acc[8 * e + 2 * h + 1] += __uint_as_float(w4[h] & 0xffff0000u) * wgt;
-                            }
-                        }
-                    }
-                    uint4* dst = (uint4*)((uint16_t*)a.out + out_row * kD + half * 64);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        uint32_t v[4];
-#pragma unroll
-                        for (int h = 0; h < 4; ++h) {
-                            const __nv_bfloat162 bb = __floats2bfloat162_rn(acc[8 * e + 2 * h], acc[8 * e + 2 * h + 1]);
-                            v[h] = *reinterpret_cast<const uint32_t*>(&bb);
-                        }
-                        dst[e] = make_uint4(v[0], v[1], v[2], v[3]);
-                    }
-                }
-                if (a.lse) a.lse[out_row] = (M + __log2f(Lsum)) * 0.69314718055994531f;
             }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float mn = M[h];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) mn = fmaxf(mn, m[h][i]);
+                const float sc = M[h] == -INFINITY ? 0.f : ex2(M[h] - mn);   // rescale the running sums
+                Ls[h] *= sc;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[h][e] *= sc;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float w = m[h][i] == -INFINITY ? 0.f : l[h][i] * ex2(m[h][i] - mn);
+                    Ls[h] += w;
+                    acc[h][0] += __uint_as_float(x[h][i].x << 16) * w;
+                    acc[h][1] += __uint_as_float(x[h][i].x & 0xffff0000u) * w;
+                    acc[h][2] += __uint_as_float(x[h][i].y << 16) * w;
+                    acc[h][3] += __uint_as_float(x[h][i].y & 0xffff0000u) * w;
+                }
+                M[h] = mn;
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int r = rr[h];
+            if (r >= rows) continue;
+            const int qi = rec.qg * kGroupRows + r, t_node = qi / G, g_head = qi - t_node * G;
+            const size_t out_row = ((size_t)rec.b * T + t_node) * a.Hq + (size_t)rec.hk * G + g_head;
+            const float inv = Ls[h] > 0.f ? 1.f / Ls[h] : 0.f;
+            const __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[h][0] * inv, acc[h][1] * inv);
+            const __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[h][2] * inv, acc[h][3] * inv);
+            ((uint2*)((uint16_t*)a.out + out_row * kD))[lane] =
+                make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1));
+            if (a.lse && lane == 0) a.lse[out_row] = (M[h] + __log2f(Ls[h])) * 0.69314718055994531f;
         }
     }
 }
@@ -727,9 +741,9 @@ bool encode_kv_map(CUtensorMap* m, const void* base, long long rows) {
 }  // namespace
 
 size_t attn_workspace_size(int B, int T, int Hq, int Hkv, int D, int kv_cap) {
-    (void)B; (void)T; (void)kv_cap;
+    (void)T; (void)kv_cap;
     if (D != kD || Hkv < 1 || Hq % Hkv) return 0;
-    return (size_t)workspace_bytes();
+    return (size_t)workspace_bytes(B);
 }
 
 bool attn_tc_supported(const AttnArgs& a) {
@@ -756,7 +770,7 @@ cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t s) {
     e = launch_ex(attn_tc_kernel, dim3(grid), dim3(kThreads), (size_t)kSmemAlloc, s, 1, false, tmK, tmV, a,
                   scale * 1.4426950408889634f);
     if (e != cudaSuccess) return e;
-    return launch_ex(attn_merge_kernel, dim3(grid), dim3(kMergeThreads), 0, s, 1, true, a, grid);
+    return launch_ex(attn_merge_kernel, dim3(grid * kMergeUnits), dim3(kMergeThreads), 0, s, 1, true, a, grid);
 }
 
 }  // namespace sv
