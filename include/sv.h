@@ -140,6 +140,29 @@ sv_status sv_accept(int B, int T, int V, sv_dtype logit_dt, const void* target_l
                     sv_stream_t stream);
 
 /*
+ * sv_accept_noalloc -- sv_accept for callers that cannot allocate device memory.
+ *
+ * The method's pages have no counterpart to this call; it is an interface convenience.  Some callers
+ * cannot hand the library a workspace: code that runs where allocation is not allowed (a serving loop
+ * whose allocator is owned by another framework, a plugin without access to an allocator, a real-time
+ * path that must never call cudaMalloc).  This entry point takes the same arguments as sv_accept minus
+ * the workspace and gives identical results; it allocates nothing.  Its scratch is a fixed 3 MiB array
+ * of static device memory inside the library, which every GPU that loads the library keeps until the
+ * process exits.
+ *   Limit: B * T <= 65536 (target rows); larger calls return SV_ERR_WORKSPACE and launch nothing.
+ *   The first call on each device looks up the array's device address on that device (with that device
+ *   current); make that first call before any CUDA stream capture.
+ *   Every call uses the same array: calls that overlap on the GPU (other streams, other host threads)
+ *   race and corrupt each other's results, so the caller must serialise them.  Nothing in the array
+ *   needs to start at zero.
+ */
+sv_status sv_accept_noalloc(int B, int T, int V, sv_dtype logit_dt, const void* target_logits,
+                            const void* draft_logits, const int32_t* tokens, const int32_t* parent,
+                            float temperature, const uint32_t* uniforms, int32_t* accept_len, int32_t* path,
+                            int32_t* out_tokens, int32_t* bonus, int32_t* argmax, int32_t* status,
+                            sv_stream_t stream);
+
+/*
  * sv_loss -- acceptance + rejection loss of the draft over N logged trees, and its gradient.
  *
  * Row (n, p) of draft_logits ([N*T, V], bf16) is the draft's logits after node p of trace n; q_p is its

@@ -19,6 +19,8 @@
 //   prefix_sum(j) > floor(U_0 * R / 2^32).
 #include <cooperative_groups.h>
 
+#include <mutex>
+
 #include "sv_internal.cuh"
 
 namespace cg = cooperative_groups;
@@ -493,7 +495,32 @@ cudaError_t launch_typed(const AcceptArgs& a, cudaStream_t s) {
     }
 }
 
+// Scratch of the allocation-free entry point: row statistics for up to kNoAllocMaxRows target rows (and as
+// many draft rows), 3 MiB of device memory that every GPU loading the library keeps until exit.
+constexpr int kNoAllocMaxRows = 65536;
+static_assert(sizeof(RowStat) == 24, "RowStat layout");
+
 }  // namespace
+
+static __device__ __align__(256) unsigned char g_accept_scratch[2ull * kNoAllocMaxRows * sizeof(RowStat)];
+
+int accept_noalloc_max_rows() { return kNoAllocMaxRows; }
+
+// Device address of the scratch array on the current device, looked up once per device with that device
+// current (host code only sees a host-side stand-in for the symbol).  nullptr if the lookup fails.
+void* accept_noalloc_scratch() {
+    static std::mutex mu;
+    static void* addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
 
 size_t accept_workspace_size(int B, int T, int V) {
     (void)V;

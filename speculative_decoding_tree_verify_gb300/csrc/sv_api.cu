@@ -98,6 +98,33 @@ sv_status sv_accept(int B, int T, int V, sv_dtype logit_dt, const void* target_l
     return from_cuda(launch_accept(a, (cudaStream_t)stream));
 }
 
+sv_status sv_accept_noalloc(int B, int T, int V, sv_dtype logit_dt, const void* target_logits,
+                            const void* draft_logits, const int32_t* tokens, const int32_t* parent,
+                            float temperature, const uint32_t* uniforms, int32_t* accept_len, int32_t* path,
+                            int32_t* out_tokens, int32_t* bonus, int32_t* argmax, int32_t* status,
+                            sv_stream_t stream) {
+    if (T > SV_MAX_T) return SV_ERR_TREE_TOO_LARGE;
+    if (B < 0 || T < 1 || V < 1) return SV_ERR_INVALID_ARG;
+    if ((long long)B * T > accept_noalloc_max_rows()) return SV_ERR_WORKSPACE;
+    if (!(temperature >= 0.f) || isinf(temperature)) return SV_ERR_INVALID_ARG;
+    if (logit_dt != SV_F32 && logit_dt != SV_BF16) return SV_ERR_UNSUPPORTED;
+    const bool stoch = temperature > 0.f;
+    if (stoch && !uniforms) return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!target_logits || !tokens || !parent || !accept_len || !path || !out_tokens || !bonus)
+        return SV_ERR_INVALID_ARG;
+    if (!aligned(target_logits, 16) || !aligned(draft_logits, 16) || !aligned(tokens, 4) || !aligned(parent, 4) ||
+        !aligned(uniforms, 4) || !aligned(accept_len, 4) || !aligned(path, 4) || !aligned(out_tokens, 4) ||
+        !aligned(bonus, 4) || !aligned(argmax, 4) || !aligned(status, 4))
+        return SV_ERR_UNSUPPORTED;
+    void* scratch = accept_noalloc_scratch();
+    if (!scratch) return SV_ERR_CUDA;
+    AcceptArgs a{B, T, V, logit_dt, target_logits, stoch ? draft_logits : nullptr, tokens, parent, temperature,
+                 stoch ? (float)(1.0 / (double)temperature) : 1.f, uniforms, accept_len, path, out_tokens,
+                 bonus, argmax, status, scratch};
+    return from_cuda(launch_accept(a, (cudaStream_t)stream));
+}
+
 sv_status sv_loss(int N, int T, int V, const void* draft_logits, const int32_t* tokens,
                   const int32_t* parent, const int32_t* labels, float* row_loss, float* sums, void* grad,
                   int32_t* status, void* workspace, size_t ws_bytes, sv_stream_t stream) {

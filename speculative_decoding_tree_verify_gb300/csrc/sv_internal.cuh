@@ -103,6 +103,8 @@ struct AcceptArgs {
 
 size_t accept_workspace_size(int B, int T, int V);
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s);
+int accept_noalloc_max_rows();
+void* accept_noalloc_scratch();
 
 struct LossArgs {
     int N, T, V;

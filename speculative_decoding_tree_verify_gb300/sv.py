@@ -47,6 +47,8 @@ def lib() -> C.CDLL:
         L.sv_accept.restype = i
         L.sv_loss.argtypes = [i, i, i, P, P, P, P, P, P, P, P, P, z, P]
         L.sv_loss.restype = i
+        L.sv_accept_noalloc.argtypes = [i, i, i, i, P, P, P, P, f, P, P, P, P, P, P, P, P]
+        L.sv_accept_noalloc.restype = i
         _lib = L
     return _lib
 
@@ -120,6 +122,17 @@ def accept(target_logits, tokens, parent, accept_len, path, out_tokens, bonus, *
                            _ptr(path), _ptr(out_tokens), _ptr(bonus), _ptr(argmax), _ptr(status), _ptr(ws),
                            ws.numel() * ws.element_size(), _stream(stream))
     _check(code, "sv_accept")
+
+
+def accept_noalloc(target_logits, tokens, parent, accept_len, path, out_tokens, bonus, *, draft_logits=None,
+                   temperature=0.0, uniforms=None, argmax=None, status=None, stream=None):
+    """sv_accept_noalloc: sv_accept using the library's built-in scratch (no workspace argument)."""
+    B, T, V = target_logits.shape
+    code = lib().sv_accept_noalloc(B, T, V, dtype_code(target_logits), _ptr(target_logits), _ptr(draft_logits),
+                                   _ptr(tokens), _ptr(parent), float(temperature), _ptr(uniforms),
+                                   _ptr(accept_len), _ptr(path), _ptr(out_tokens), _ptr(bonus), _ptr(argmax),
+                                   _ptr(status), _stream(stream))
+    _check(code, "sv_accept_noalloc")
 
 
 def loss(draft_logits, tokens, parent, labels, row_loss, sums, *, grad=None, status=None, workspace=None,
