@@ -316,7 +316,9 @@ def run_sv(args, rank, world, local_rank):
     else:
         dom, byt, t_dom, src = "accept", cb, t_acc, ROOT / "speculative_decoding_tree_verify_gb300/csrc/accept.cu"
     achieved = byt / (t_dom * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "kernel": dom + (" (planner + attn_tc_kernel)" if dom == "tree_attn" and tc else ""), "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
+    label = {"tree_attn": "sv_tree_attn (attn_tc_kernel + attn_merge_kernel)" if tc else "sv_tree_attn (attn_simt_kernel)",
+             "accept": "sv_accept (accept_rows_kernel + accept_walk_kernel)"}[dom]
+    roofline = {"bound": "hbm", "kernel": label, "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
                 "unit": "GB/s", "frac": achieved / peak, "algorithmic_bytes_per_launch": byt,
                 "traffic": traffic_from_profile(src, args.workload),
                 "step_frac": (ab + cb) / (ms * 1e-3) / 1e9 / peak}
@@ -324,7 +326,7 @@ def run_sv(args, rank, world, local_rank):
     if not args.no_cpu_baseline:
         v, cores, desc = cpu_oracle_sample(w, args.cpu_seconds)
         cpu = {"value": v, "unit": "nodes/s", "cores": cores, "kind": "oracle", "sample": desc}
-    launches_per_step = (2 if tc else 1) + 2     # [planner +] attention kernel, accept rows + walk
+    launches_per_step = (2 if tc else 1) + 2     # attention [+ merge], accept rows + walk
     line = {"metric": METRIC, "value": value, "unit": "nodes/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": w.q_dt, "data": "synthetic",
