@@ -34,6 +34,7 @@
 // (bounded) for its own copies and MMAs before it frees TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
 
 #include "sv_internal.cuh"
 #include "tc_ptx.cuh"
@@ -46,7 +47,9 @@ using namespace tc;
 constexpr int kD = 128;
 constexpr int kTileN = 128;                      // kv positions per tile
 constexpr int kRows = 128;                       // query rows per CTA (one M tile)
-constexpr int kStages = 6;                       // ring slots (one K or one V tile each)
+constexpr int kRingMax = 6;                      // ring slots (one K or one V tile each): 6 for bf16 KV, 4 for e4m3
+constexpr int kStage8 = 4;                       // e4m3 staging slots (FP8 KV only)
+constexpr int kSlot8Bytes = kTileN * kD;         // 16 KB: one e4m3 K or V tile
 constexpr int kSlotBytes = kTileN * kD * 2;      // 32 KB
 constexpr int kBoxBytes = kSlotBytes / 2;        // one 64-column box: 128 rows x 128 bytes
 constexpr int kThreads = 384;
@@ -54,8 +57,10 @@ constexpr int kMaxGrid = 160;                    // the workspace is sized for g
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
 constexpr int kMergeThreads = 256;               // 8 warps
 
-constexpr int kSmemRing = 0;                     // [6][32 KB]
-constexpr int kSmemBytes = kSmemRing + kStages * kSlotBytes;   // 196608
+constexpr int kSmemRing = 0;                     // bf16 KV: [6][32 KB]; FP8 KV: [4][32 KB] f16 slots, then
+constexpr int kSmemStage = 4 * kSlotBytes;       //   the e4m3 staging slots [4][16 KB]
+constexpr int kSmemBytes = 6 * kSlotBytes;       // 196608 either way
+static_assert(kSmemStage + kStage8 * kSlot8Bytes == kSmemBytes, "FP8 smem layout");
 constexpr int kSmemAlloc = kSmemBytes + 1024;                  // + alignment slack
 
 // TMEM columns (32-bit, one lane per query row): O at 0 (128 columns), S at 128 (128 columns, one buffer:
@@ -91,6 +96,25 @@ __device__ __forceinline__ float max3(float x, float y, float z) {
     float r;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(x), "f"(y), "f"(z));
     return r;
+}
+
+// two e4m3 (low byte -> low half) to two f16, exactly
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+    return r;
+}
+
+// two floats to a bf16 or f16 pair (the first in the low half)
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (F16) {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    } else {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -237,7 +261,8 @@ struct SegIter {
 
 // ------------------------------------------------------------------------------------------------ main kernel
 struct MainShared {
-    uint64_t full[kStages], empty[kStages];
+    uint64_t full[kRingMax], empty[kRingMax];
+    uint64_t full8[kStage8], empty8[kStage8];              // e4m3 staging (FP8 KV only)
     uint64_t s_full, s_free, p_full[kPBufs], pv_done[kPBufs];  // P barriers per P buffer
     uint64_t q_full, o_full, drain[2];
     Plan plan;
@@ -249,10 +274,14 @@ struct MainShared {
     int err;
 };
 
-template <int CL>
+// KV8: the caches hold e4m3.  The producer then loads e4m3 tiles into a staging ring, warp 3 converts them
+// exactly to f16 (every e4m3 value is an f16 value) into the MMA ring, and the MMAs run on f16 operands
+// (Q and P rounded to f16); k_scale is folded into the softmax scale and v_scale into the epilogue.
+template <int CL, bool KV8>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, AttnArgs a,
                float scale_log2) {
+    constexpr int kStages = KV8 ? 4 : kRingMax;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     __shared__ MainShared sh;
@@ -269,6 +298,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&sh.full[i], 1);
             mbar_init(&sh.empty[i], CL);             // one release per CTA of the cluster
+        }
+        for (int i = 0; i < kStage8; ++i) {
+            mbar_init(&sh.full8[i], 1);
+            mbar_init(&sh.empty8[i], 1);
         }
         mbar_init(&sh.s_full, 1);
         mbar_init(&sh.s_free, 8);                    // one arrival per softmax warp
@@ -308,6 +341,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             while (!*err && si.next(sg)) {
                 const int row0 = (sg.b * a.Hkv + sg.hk) * a.kv_cap;
                 for (int t = sg.t0; t < sg.t1 && !*err; ++t) {
+                    if constexpr (KV8) {
+                        // e4m3 K and V tiles into the staging ring (one 16 KB box each)
+                        for (int kv = 0; kv < 2; ++kv, ++use) {
+                            const uint32_t slot = use % kStage8, round = use / kStage8;
+                            if (!mbar_wait(&sh.empty8[slot], (round & 1) ^ 1, err)) break;
+                            mbar_arrive_expect_tx(&sh.full8[slot], kSlot8Bytes);
+                            tma_load_2d(smem + kSmemStage + slot * kSlot8Bytes, kv ? (const void*)&tmV : (const void*)&tmK,
+                                        0, row0 + t * kTileN, &sh.full8[slot]);
+                        }
+                        continue;
+                    }
                     for (int kv = 0; kv < 2; ++kv, ++use) {
                         const uint32_t slot = use % kStages, round = use / kStages;
                         // the slot is free in every CTA of the cluster
@@ -330,15 +374,62 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             // wait (bounded) until every CTA of the cluster has released the last slots, so no copy or
             // remote release is still in flight towards this CTA when it exits
             volatile int local = 0;
-            const uint32_t first_u = use > (uint32_t)kStages ? use - kStages : 0;
-            for (uint32_t u = first_u; u < use && !local; ++u) mbar_wait(&sh.empty[u % kStages], (u / kStages) & 1, &local);
+            const uint32_t nring = KV8 ? kStage8 : kStages;
+            const uint32_t first_u = use > nring ? use - nring : 0;
+            for (uint32_t u = first_u; u < use && !local; ++u)
+                mbar_wait(KV8 ? &sh.empty8[u % nring] : &sh.empty[u % nring], (u / nring) & 1, &local);
+        }
+    } else if (warp == 3) {
+        // ---------------------------------------------------------------- e4m3 -> f16 converter (FP8 KV)
+        if (KV8 && active) {
+            uint32_t use = 0;
+            SegIter si;
+            si.init(a, plan, UQ, QG);
+            Seg sg;
+            bool ok = true;
+            while (ok && !*err && si.next(sg)) {
+                for (int t = sg.t0; t < sg.t1 && ok; ++t) {
+                    for (int kv = 0; kv < 2 && ok; ++kv, ++use) {
+                        const uint32_t s8 = use % kStage8, s16 = use % kStages;
+                        ok = __all_sync(0xffffffffu, mbar_wait(&sh.full8[s8], (use / kStage8) & 1, err));
+                        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&sh.empty[s16], ((use / kStages) & 1) ^ 1, err));
+                        if (!ok) break;
+                        const uint8_t* src = smem + kSmemStage + s8 * kSlot8Bytes;
+                        uint8_t* dst = smem + kSmemRing + s16 * kSlotBytes;
+                        // chunk j: row j / 8, e4m3 bytes 16 (j % 8) .. +15 -> f16 d 16 (j % 8) .. +15, which is
+                        // box (j % 8) / 4, 16-byte chunks 2 (j % 4) and 2 (j % 4) + 1 of that row
+#pragma unroll 4
+                        for (int j = lane; j < kTileN * 8; j += 32) {
+                            const int r = j >> 3, c = j & 7;
+                            const uint4 w = *(const uint4*)(src + r * 128 + c * 16);
+                            const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+                            uint32_t hf[8];
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                hf[2 * q] = e4m3x2_to_f16x2((uint16_t)(wv[q] & 0xffffu));
+                                hf[2 * q + 1] = e4m3x2_to_f16x2((uint16_t)(wv[q] >> 16));
+                            }
+                            uint8_t* box = dst + (c >> 2) * kBoxBytes;
+                            *(uint4*)(box + sw128_offset(r, 2 * (c & 3))) = make_uint4(hf[0], hf[1], hf[2], hf[3]);
+                            *(uint4*)(box + sw128_offset(r, 2 * (c & 3) + 1)) = make_uint4(hf[4], hf[5], hf[6], hf[7]);
+                        }
+                        fence_proxy_async_smem();   // the MMAs (async proxy) read what this warp wrote
+                        __syncwarp();
+                        if (lane == 0) {
+                            mbar_arrive(&sh.full[s16]);
+                            mbar_arrive(&sh.empty8[s8]);
+                        }
+                    }
+                }
+            }
         }
     } else if (warp == 1 || warp == 2) {
         // ---------------------------------------------------------------- MMA issuers: S (warp 1), PV (warp 2)
         const bool is_s = warp == 1;
         if (lane == 0 && active) {
-            const uint32_t idS = idesc_bf16_f32(128, kTileN, false, false);   // A (Q) from TMEM, K-major B
-            const uint32_t idO = idesc_bf16_f32(128, kD, false, true);
+            // A (Q, P) from TMEM; B (K, V) from shared memory; f16 operands for FP8 KV, bf16 otherwise
+            const uint32_t idS = KV8 ? idesc_f16_f32(128, kTileN, false, false) : idesc_bf16_f32(128, kTileN, false, false);
+            const uint32_t idO = KV8 ? idesc_f16_f32(128, kD, false, true) : idesc_bf16_f32(128, kD, false, true);
             const uint64_t dK = sdesc_sw128(0, 16, 1024);          // K-major operands (Q, K)
             const uint64_t dV = sdesc_sw128(0, kBoxBytes, 1024);   // MN-major V: next 64 d one box further
             auto at = [](uint64_t base, uint32_t saddr) { return base | (uint64_t)((saddr & 0x3FFFFu) >> 4); };
@@ -427,6 +518,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             const uint32_t use0 = use;
             use += 2u * nt;
             const int L = __ldg(a.kv_len + b);
+            // softmax scale in log2 units (times k_scale for e4m3 K); output scale (v_scale for e4m3 V)
+            const float sc = KV8 ? scale_log2 * __ldg(a.k_scale + hk) : scale_log2;
+            const float osc = KV8 ? __ldg(a.v_scale + hk) : 1.f;
             const int row0 = sg.qg * kUnitRows + rank * kRows;     // first query row of this M tile
             const int qi = row0 + row;
             const bool valid_row = qi < TG;
@@ -467,7 +561,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 }
             }
             dead = __any_sync(0xffffffffu, dead || *err);
-            // this warp's half (64 of 128 d) of the Q rows -> TMEM, bf16 pairs (even d in the low half)
+            // this warp's half (64 of 128 d) of the Q rows -> TMEM, pairs with the even d in the low half (bf16, or
+            // rounded to f16 when the caches are e4m3)
             if (!dead) {
                 const uint4* src = (const uint4*)((const uint16_t*)a.q + out_row * kD) + 8 * h;
                 uint32_t qv[32];
@@ -478,6 +573,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                     qv[4 * c + 1] = v.y;
                     qv[4 * c + 2] = v.z;
                     qv[4 * c + 3] = v.w;
+                }
+                if constexpr (KV8) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        qv[c] = pack2<true>(__uint_as_float(qv[c] << 16), __uint_as_float(qv[c] & 0xffff0000u));
                 }
                 __syncwarp();
                 tmem_st32(tmem + lane_addr + col_Q() + 32 * h, qv);
@@ -539,18 +639,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 float ps[4], alpha = 1.f, m_use = m_run;
                 auto exps = [&](float m) {
                     const bool live = m != -INFINITY;
-                    const float moff = live ? -m * scale_log2 : 0.f;
+                    const float moff = live ? -m * sc : 0.f;
                     ps[0] = ps[1] = ps[2] = ps[3] = 0.f;
 #pragma unroll
                     for (int part2 = 0; part2 < 2; ++part2) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int c = 0; c < 16; ++c) {
-                            const float p0 = live ? ex2(fmaf(s[32 * part2 + 2 * c], scale_log2, moff)) : 0.f;
-                            const float p1 = live ? ex2(fmaf(s[32 * part2 + 2 * c + 1], scale_log2, moff)) : 0.f;
+                            const float p0 = live ? ex2(fmaf(s[32 * part2 + 2 * c], sc, moff)) : 0.f;
+                            const float p1 = live ? ex2(fmaf(s[32 * part2 + 2 * c + 1], sc, moff)) : 0.f;
                             ps[c & 3] += p0 + p1;
-                            const __nv_bfloat162 hb = __floats2bfloat162_rn(p0, p1);
-                            pk[c] = *reinterpret_cast<const uint32_t*>(&hb);
+                            pk[c] = pack2<KV8>(p0, p1);
                         }
                         __syncwarp();
                         if (!dead) tmem_st16(tmem + lane_addr + col_P(bb) + 32 * h + 16 * part2, pk);
@@ -567,12 +666,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 sh.xch[gi & 1][h][row] = tmax_h;   // double-buffered by tile parity: one barrier per tile
                 pair_sync();
                 const float tmax = fmaxf(tmax_h, sh.xch[gi & 1][h ^ 1][row]);
-                if (!slow) slow = __any_sync(0xffffffffu, valid_row && (tmax - m_run) * scale_log2 > kRescaleThreshold);
+                if (!slow) slow = __any_sync(0xffffffffu, valid_row && (tmax - m_run) * sc > kRescaleThreshold);
                 if (slow) {
                     const float m_new = fmaxf(m_run, tmax);
-                    const bool rescale = m_run != -INFINITY && (m_new - m_run) * scale_log2 > kRescaleThreshold;
+                    const bool rescale = m_run != -INFINITY && (m_new - m_run) * sc > kRescaleThreshold;
                     m_use = (m_run == -INFINITY || rescale) ? m_new : m_run;
-                    alpha = rescale ? ex2((m_run - m_use) * scale_log2) : 1.f;
+                    alpha = rescale ? ex2((m_run - m_use) * sc) : 1.f;
                     // O holds PV of the previous tile: wait for it, then rescale this warp's half of O
                     if (__any_sync(0xffffffffu, rescale) && wait(&sh.pv_done[(gi - 1) % kPBufs], ((gi - 1) / kPBufs) & 1)) {
                         tc_fence_after();
@@ -621,9 +720,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             pair_sync();
             const float l_tot = l_run + sh.lx[h ^ 1][row];
             if (!dead) {
-                const float m_log2 = m_run * scale_log2;
+                const float m_log2 = m_run * sc;
                 // normalised O (bf16, this warp's 64 d columns) either to the output row or to the partial slot
-                const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
+                const float inv_l = l_tot > 0.f ? osc / l_tot : 0.f;
                 uint16_t* dst_row = (part ? (uint16_t*)part + (size_t)row * kD : (uint16_t*)a.out + out_row * kD) + 64 * h;
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
@@ -800,21 +899,24 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-bool encode_kv_map(CUtensorMap* m, const void* base, long long rows) {
+// bf16 caches: boxes of 64 columns x 128 rows, 128-byte swizzle (the MMA layout).  e4m3 caches: whole
+// 128-byte rows x 128 rows, unswizzled (the converter's input).
+bool encode_kv_map(CUtensorMap* m, const void* base, long long rows, bool e4m3) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-    cuuint32_t box[2] = {64, kTileN};
+    cuuint64_t strides[1] = {(cuuint64_t)kD * (e4m3 ? 1 : 2)};
+    cuuint32_t box[2] = {e4m3 ? (cuuint32_t)kD : 64u, kTileN};
     cuuint32_t es[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return enc(m, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+               dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               e4m3 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Clusters of CL CTAs that fit on the device at once with this kernel's resources (cached per CL); the
 // persistent grid never exceeds it, so every cluster of the grid is resident from the start.
-template <int CL>
+template <int CL, bool KV8>
 int resident_clusters() {
     static int n = 0;
     if (!n) {
@@ -830,28 +932,28 @@ int resident_clusters() {
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
         int c = 0;
-        if (cudaOccupancyMaxActiveClusters(&c, attn_tc_kernel<CL>, &cfg) != cudaSuccess || c < 1) c = num_sms() / CL;
+        if (cudaOccupancyMaxActiveClusters(&c, attn_tc_kernel<CL, KV8>, &cfg) != cudaSuccess || c < 1) c = num_sms() / CL;
         n = c;
     }
     return n;
 }
 
-template <int CL>
+template <int CL, bool KV8>
 cudaError_t launch_main(const AttnArgs& a, cudaStream_t s, float scale_log2, int* grid_out) {
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<CL, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     CUtensorMap tmK, tmV;
     const long long rows = (long long)a.B * a.Hkv * a.kv_cap;
-    if (!encode_kv_map(&tmK, a.k, rows) || !encode_kv_map(&tmV, a.v, rows)) return cudaErrorInvalidValue;
-    int ncl = resident_clusters<CL>();
+    if (!encode_kv_map(&tmK, a.k, rows, KV8) || !encode_kv_map(&tmV, a.v, rows, KV8)) return cudaErrorInvalidValue;
+    int ncl = resident_clusters<CL, KV8>();
     if (ncl * CL > kMaxGrid) ncl = kMaxGrid / CL;
     *grid_out = ncl * CL;
-    return launch_ex(attn_tc_kernel<CL>, dim3(ncl * CL), dim3(kThreads), (size_t)kSmemAlloc, s, CL, false, tmK, tmV,
-                     a, scale_log2);
+    return launch_ex(attn_tc_kernel<CL, KV8>, dim3(ncl * CL), dim3(kThreads), (size_t)kSmemAlloc, s, CL, false, tmK,
+                     tmV, a, scale_log2);
 }
 
 }  // namespace
@@ -862,10 +964,16 @@ size_t attn_workspace_size(int B, int T, int Hq, int Hkv, int D, int kv_cap) {
     return (size_t)workspace_bytes();
 }
 
+// Units of two M tiles (2-CTA clusters sharing multicast tiles) for bf16 caches with more than 128 query
+// rows per kv head; units of one M tile otherwise (e4m3 caches: every CTA converts its own tiles).
+int cluster_size(const AttnArgs& a) {
+    return (a.kv_dt == SV_BF16 && (long long)a.T * (a.Hq / a.Hkv) > kRows) ? 2 : 1;
+}
+
 bool attn_tc_supported(const AttnArgs& a) {
     const long long TG = (long long)a.T * (a.Hq / a.Hkv);
-    const long long unit_rows = TG > kRows ? 2 * kRows : kRows;
-    return a.q_dt == SV_BF16 && a.kv_dt == SV_BF16 && a.D == kD && a.B >= 1 &&
+    const long long unit_rows = (long long)cluster_size(a) * kRows;
+    return a.q_dt == SV_BF16 && (a.kv_dt == SV_BF16 || a.kv_dt == SV_E4M3) && a.D == kD && a.B >= 1 &&
            (long long)a.B * a.Hkv * a.kv_cap < (1LL << 31) - kTileN && TG < 65536 &&
            // tile indices of the whole call fit the kernel's 32-bit bookkeeping
            (long long)a.B * a.Hkv * ((TG + unit_rows - 1) / unit_rows) * ((a.kv_cap + kTileN - 1) / kTileN) < (1LL << 24) &&
@@ -877,10 +985,11 @@ cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t s) {
     cudaError_t e = cudaMemsetAsync(a.ws, 0, 4, s);
     if (e != cudaSuccess) return e;
     const float scale = a.sm_scale != 0.f ? a.sm_scale : (float)(1.0 / sqrt((double)a.D));
-    const int CL = (long long)a.T * (a.Hq / a.Hkv) > kRows ? 2 : 1;
+    const int CL = cluster_size(a);
+    const float sl2 = scale * 1.4426950408889634f;
     int grid = 0;
-    e = CL == 2 ? launch_main<2>(a, s, scale * 1.4426950408889634f, &grid)
-                : launch_main<1>(a, s, scale * 1.4426950408889634f, &grid);
+    if (a.kv_dt == SV_E4M3) e = launch_main<1, true>(a, s, sl2, &grid);
+    else e = CL == 2 ? launch_main<2, false>(a, s, sl2, &grid) : launch_main<1, false>(a, s, sl2, &grid);
     if (e != cudaSuccess) return e;
     return launch_ex(attn_merge_kernel, dim3(grid * kMergeUnits), dim3(kMergeThreads), 0, s, 1, true, a, grid, CL);
 }
