@@ -98,3 +98,33 @@ def test_named_small_workload_full(name):
 @pytest.mark.parametrize("name", ["llama3_8b_tree", "qwen3_8b_stochastic"])
 def test_named_workloads_full_size_sampled(name):
     check_sampled(W.make_workload(name, seed=0))
+
+
+# E4M3 caches with bf16 Q and D = 128 run on the tensor cores (e4m3 -> f16 conversion in shared memory):
+# ragged prefixes, trees up to 64 nodes, and config-5 head shapes, with NaN junk past every tree block.
+FP8_TC = [
+    # B, T, Hq, Hkv, L, tree
+    (1, 1, 4, 4, (0, 0), "chain"),
+    (2, 6, 8, 2, (100, 300), "chain"),
+    (3, 13, 16, 2, (1, 700), (3, 2, 2)),
+    (2, 60, 32, 8, (2048, 3000), (4, 3, 2, 2, 1, 1)),
+    (2, 64, 64, 8, (8192, 9000), (4, 3, 2, 2, 1, 1, 1)),
+]
+
+
+@pytest.mark.parametrize("case", FP8_TC)
+def test_attn_fp8_tensor_core_parity(case):
+    B, T, Hq, Hkv, L, tree = case
+    w = W.make_verify(300 + sum(L) + T, B=B, T=T, Hq=Hq, Hkv=Hkv, D=128, L=L, V=64, q_dt="bf16", kv_dt="e4m3",
+                      tree=tree, junk="nan")
+    if B * T * Hq > 4000:
+        check_sampled(w)
+    else:
+        out, _ = check_full(w)
+        assert np.isfinite(out).all()
+
+
+def test_fp8_long_context_attention_sampled():
+    # config-5 requests (T=64, 64/8 heads, e4m3 KV, L in [8192, 32768]) at 16 requests, the most whose caches
+    # the host generator can build for the oracle in a test
+    check_sampled(W.make_workload("fp8_long_context", seed=0, B=16))
