@@ -56,23 +56,63 @@ __device__ __forceinline__ float fx_exp2_poly(float f) {
     return p;
 }
 
+// W = 0 if t < -24, else floor(P(t - rint t) * 2^(24 + rint t)), t = (y - m) * log2(e).  rint comes from
+// the 1.5 * 2^23 rounding constant (round half to even, exact for |t| < 2^22), which also leaves n in the
+// low bits of the sum, so only the final floor needs a conversion instruction.
 __device__ __forceinline__ uint32_t fx_weight(float y, float m) {
-    float t = __fmul_rn(__fsub_rn(y, m), 0x1.715476p+0f);
+    const float t = __fmul_rn(__fsub_rn(y, m), 0x1.715476p+0f);
     if (!(t >= -24.0f)) return 0u;
-    float n = rintf(t);
-    float f = __fsub_rn(t, n);
-    float scale = __uint_as_float((uint32_t)(127 + 24 + (int)n) << 23);   // 2^(24+n), exact
+    const float r = __fadd_rn(t, 12582912.0f);                     // 1.5 * 2^23 + rint(t), exactly
+    const int n = (int)__float_as_uint(r) - 0x4B400000;            // rint(t) in [-24, 0]
+    const float f = __fsub_rn(t, __fsub_rn(r, 12582912.0f));
+    const float scale = __uint_as_float((uint32_t)(127 + 24 + n) << 23);   // 2^(24+n), exact
     return __float2uint_rd(__fmul_rn(fx_exp2_poly(f), scale));
 }
 
-// floor(n / d) for n < 2^70, d >= 1, quotient < 2^26: double estimate, then one exact correction step.
-__device__ __forceinline__ u64 udiv_small_quotient(u128 n, u64 d) {
-    double qd = (double)n / (double)d;
-    u64 q = (u64)qd;
-    u128 prod = (u128)q * d;
-    if (prod > n) --q;
-    else if (prod + d <= n) ++q;
+// One rejection step of the residual, exactly in integers:
+//   floor(max(0, w * d - wq * X) / d)  =  max(0, w - ceil(wq * X / d)),
+// with X = a * d + b (b < d) and F = floor(2^64 * b / d) prepared once per rejection.  For wq <= 2^25,
+// floor(wq * b / d) is umulhi(wq, F) or one more, decided by an exact 128-bit product; no division and no
+// double precision per token.
+struct ResidStep {
+    u64 a, b, F;
+};
+
+// floor(2^64 * b / d) for b < d < 2^62, by restoring division (once per rejection)
+__device__ u64 frac64(u64 b, u64 d) {
+    u64 q = 0, r = b;
+    for (int i = 0; i < 64; ++i) {
+        r <<= 1;
+        q <<= 1;
+        if (r >= d) {
+            r -= d;
+            q |= 1u;
+        }
+    }
     return q;
+}
+
+// x * y for x < 2^32 as a 128-bit value, from two 32 x 32 -> 64-bit products
+__device__ __forceinline__ u128 mul_32x64(uint32_t x, u64 y) {
+    return (u128)((u64)x * (uint32_t)y) + ((u128)((u64)x * (uint32_t)(y >> 32)) << 32);
+}
+
+__device__ __forceinline__ u64 resid_step(u64 w, u64 wq64, const ResidStep& k, u64 d) {
+    const uint32_t wq = (uint32_t)wq64;   // a weight: at most 2^24
+    const u64 q0 = (u64)(mul_32x64(wq, k.F) >> 64);
+    const u128 num = mul_32x64(wq, k.b);
+    const u128 m1 = mul_32x64((uint32_t)(q0 + 1), d);
+    u64 q;
+    bool exact;
+    if (num >= m1) {
+        q = q0 + 1;
+        exact = num == m1;
+    } else {
+        q = q0;
+        exact = num == mul_32x64((uint32_t)q0, d);
+    }
+    const u64 c = (u64)wq * k.a + q + (exact ? 0u : 1u);
+    return w > c ? w - c : 0u;
 }
 
 template <int LDT> struct Logit;
@@ -246,6 +286,7 @@ struct WalkShared {
     int32_t tok[SV_MAX_T];
     int32_t path[SV_MAX_T];
     u64 hist[SV_MAX_T];       // PROB: residual sum before each rejection; ONEHOT: rejected tokens
+    ResidStep rs[SV_MAX_T];   // PROB: the integer constants of each rejection step
     u64 red[kWalkThreads / 32];
     u64 cta_sum;              // this CTA's share of a cluster-wide sum (read remotely)
     int32_t found;            // sampled index found in this CTA (-1 if not)
@@ -253,11 +294,13 @@ struct WalkShared {
 };
 
 template <int LDT, int MODE>
-__global__ void __launch_bounds__(kWalkThreads) accept_walk_kernel(AcceptArgs a, int CLW) {
+__global__ void __launch_bounds__(kWalkThreads, 2) accept_walk_kernel(AcceptArgs a, int CLW) {
     using LG = Logit<LDT>;
     using LT = typename LG::T;
+    constexpr int VEC = LG::kVec;
     cg::cluster_group cluster = cg::this_cluster();
     __shared__ WalkShared sh;
+    const bool vec_ok = (a.V % VEC) == 0;   // every logit row 16-byte aligned (base checked on the host)
     const int rank = (int)cluster.block_rank();
     const int b = blockIdx.x / CLW;
     const int T = a.T, V = a.V, B = a.B;
@@ -335,23 +378,62 @@ __global__ void __launch_bounds__(kWalkThreads) accept_walk_kernel(AcceptArgs a,
             const LT* prow_q = (MODE == MODE_PROB) ? Q + prow * V : nullptr;
             int nrej = 0;
             u64 Sres = sp.S;
-            // residual weight of token k after the rejections so far
-            auto wres = [&](int k) -> u64 {
-                u64 w = fx_weight(__fmul_rn(LG::load(prow_p + k), invT), sp.ymax);
+            // residual weight of token k (target logit zp, draft logit zq) after the rejections so far
+            auto wres_z = [&](float zp, float zq, int k) -> u64 {
+                u64 w = fx_weight(__fmul_rn(zp, invT), sp.ymax);
                 if (MODE == MODE_ONEHOT) {
                     for (int i = 0; i < nrej; ++i) if ((int)sh.hist[i] == k) w = 0;
                 } else if (MODE == MODE_PROB) {
                     if (nrej) {
-                        u64 wq = fx_weight(__fmul_rn(LG::load(prow_q + k), invT), sq.ymax);
-                        for (int i = 0; i < nrej; ++i) {
-                            u128 x = (u128)w * Sq, s = (u128)wq * sh.hist[i];
-                            w = x > s ? udiv_small_quotient(x - s, Sq) : 0;
-                        }
+                        const u64 wq = fx_weight(__fmul_rn(zq, invT), sq.ymax);
+                        for (int i = 0; i < nrej; ++i) w = resid_step(w, wq, sh.rs[i], Sq);
                     }
                 }
                 return w;
             };
+            auto wres = [&](int k) -> u64 {
+                return wres_z(LG::load(prow_p + k), MODE == MODE_PROB ? LG::load(prow_q + k) : 0.f, k);
+            };
+            // the VEC residual weights of tokens k .. k+VEC-1 (16-byte loads; rows are 16-byte aligned)
+            auto wres_vec = [&](int k, u64 (&w)[VEC]) {
+                float zp[VEC], zq[VEC];
+                LG::load_vec(prow_p + k, zp);
+                if (MODE == MODE_PROB) LG::load_vec(prow_q + k, zq);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) w[e] = wres_z(zp[e], MODE == MODE_PROB ? zq[e] : 0.f, k + e);
+            };
+            // Cluster layout of the vocabulary: CTA `rank` owns [k0, k1), its warp w the contiguous segment
+            // [s0, s1) (whole vectors when vectorised).  seg_sums() leaves each warp's residual mass in
+            // sh.red[w] and the CTA's in sh.cta_sum; the bonus draw then searches CTA, warp and token in order.
+            const int per = vec_ok ? ((V + CLW - 1) / CLW + VEC - 1) / VEC * VEC : (V + CLW - 1) / CLW;
+            const int k0 = min(V, rank * per), k1 = min(V, k0 + per);
+            const int nw = kWalkThreads / 32;
+            const int seg = vec_ok ? ((k1 - k0 + nw - 1) / nw + VEC - 1) / VEC * VEC : (k1 - k0 + nw - 1) / nw;
+            const int s0 = min(k1, k0 + warp * seg), s1 = min(k1, s0 + seg);
+            auto seg_sums = [&]() {
+                u64 ws = 0;
+                if (vec_ok) {
+                    for (int k = s0 + lane * VEC; k < s1; k += 32 * VEC) {
+                        u64 w[VEC];
+                        wres_vec(k, w);
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) ws += w[e];
+                    }
+                } else {
+                    for (int k = s0 + lane; k < s1; k += 32) ws += wres(k);
+                }
+                ws = warp_sum_u64(ws);
+                if (lane == 0) sh.red[warp] = ws;
+                __syncthreads();
+                if (tid == 0) {
+                    u64 t = 0;
+                    for (int w = 0; w < nw; ++w) t += sh.red[w];
+                    sh.cta_sum = t;
+                }
+            };
+            bool sums_valid = false;   // sh.red / sh.cta_sum hold the current residual
             int next = -1, has_child = 0;
+            sums_valid = false;
             for (int c = cur + 1; c < T; ++c) {
                 if (sh.par[c] != cur) continue;
                 has_child = 1;
@@ -364,27 +446,22 @@ __global__ void __launch_bounds__(kWalkThreads) accept_walk_kernel(AcceptArgs a,
                     ++nrej;
                     Sres -= wpx;
                 } else {
-                    if (tid == 0) sh.hist[nrej] = Sres;
+                    if (tid == 0) {
+                        sh.hist[nrej] = Sres;
+                        ResidStep k;
+                        k.a = Sres / Sq;
+                        k.b = Sres - k.a * Sq;
+                        k.F = frac64(k.b, Sq);
+                        sh.rs[nrej] = k;
+                    }
                     __syncthreads();
                     ++nrej;
-                    Sres = 0;  // recomputed below
-                    {
-                        const int per = (V + CLW - 1) / CLW;
-                        const int k0 = min(V, rank * per), k1 = min(V, k0 + per);
-                        u64 s = 0;
-                        for (int k = k0 + tid; k < k1; k += kWalkThreads) s += wres(k);
-                        s = warp_sum_u64(s);
-                        if (lane == 0) sh.red[warp] = s;
-                        __syncthreads();
-                        if (tid == 0) {
-                            u64 t = 0;
-                            for (int w = 0; w < kWalkThreads / 32; ++w) t += sh.red[w];
-                            sh.cta_sum = t;
-                        }
-                        cluster.sync();
-                        for (int q = 0; q < CLW; ++q) Sres += *cluster.map_shared_rank(&sh.cta_sum, q);
-                        cluster.sync();
-                    }
+                    Sres = 0;  // recomputed below, in the layout the bonus draw searches
+                    seg_sums();
+                    cluster.sync();
+                    for (int q = 0; q < CLW; ++q) Sres += *cluster.map_shared_rank(&sh.cta_sum, q);
+                    cluster.sync();
+                    sums_valid = true;
                 }
             }
             if (next >= 0) {
@@ -399,23 +476,9 @@ __global__ void __launch_bounds__(kWalkThreads) accept_walk_kernel(AcceptArgs a,
             const u64 R = use_res ? Sres : sp.S;
             if (!use_res) nrej = 0;
             const u128 thr = ((u128)U[0] * R) >> 32;
-            const int per = (V + CLW - 1) / CLW;
-            const int k0 = min(V, rank * per), k1 = min(V, k0 + per);
-            // per-warp contiguous segments of this CTA's slice
-            const int nw = kWalkThreads / 32;
-            const int seg = (k1 - k0 + nw - 1) / nw;
-            const int s0 = min(k1, k0 + warp * seg), s1 = min(k1, s0 + seg);
-            u64 ws = 0;
-            for (int k = s0 + lane; k < s1; k += 32) ws += wres(k);
-            ws = warp_sum_u64(ws);
-            if (lane == 0) sh.red[warp] = ws;
-            __syncthreads();
-            if (tid == 0) {
-                u64 t = 0;
-                for (int w = 0; w < nw; ++w) t += sh.red[w];
-                sh.cta_sum = t;
-                sh.found = -1;
-            }
+            // the last residual pass already left the sums of the residual the draw uses
+            if (!(use_res && sums_valid)) seg_sums();
+            if (tid == 0) sh.found = -1;
             cluster.sync();
             u64 before = 0;   // weight mass of the CTAs before this one
             for (int q = 0; q < rank; ++q) before += *cluster.map_shared_rank(&sh.cta_sum, q);
@@ -427,7 +490,40 @@ __global__ void __launch_bounds__(kWalkThreads) accept_walk_kernel(AcceptArgs a,
                     if (thr < wb + sh.red[w]) { wsel = w; break; }
                     wb += sh.red[w];
                 }
-                if (warp == wsel) {
+                if (warp == wsel && vec_ok) {
+                    // 32 * VEC tokens per step: each lane one vector, a warp scan of the lane totals
+                    u64 run = wb;
+                    for (int kb = s0; kb < s1; kb += 32 * VEC) {
+                        const int k = kb + lane * VEC;
+                        u64 w[VEC];
+                        u64 tl = 0;
+                        if (k < s1) {
+                            wres_vec(k, w);
+#pragma unroll
+                            for (int e = 0; e < VEC; ++e) tl += w[e];
+                        }
+                        u64 incl = tl;
+#pragma unroll
+                        for (int o = 1; o < 32; o <<= 1) {
+                            const u64 v = __shfl_up_sync(0xffffffffu, incl, o);
+                            if (lane >= o) incl += v;
+                        }
+                        const unsigned hit = __ballot_sync(0xffffffffu, k < s1 && (u128)run + incl > thr);
+                        if (hit) {
+                            if (lane == __ffs(hit) - 1) {
+                                u128 acc = (u128)run + (incl - tl);
+                                int e = 0;
+                                for (; e < VEC - 1; ++e) {
+                                    acc += w[e];
+                                    if (acc > thr) break;
+                                }
+                                sh.found = k + e;
+                            }
+                            break;
+                        }
+                        run += __shfl_sync(0xffffffffu, incl, 31);
+                    }
+                } else if (warp == wsel) {
                     u64 run = wb;
                     for (int k = s0; k < s1; k += 32) {
                         u64 w = (k + lane < s1) ? wres(k + lane) : 0;
