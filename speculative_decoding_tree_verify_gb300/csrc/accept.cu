@@ -69,6 +69,56 @@ __device__ __forceinline__ uint32_t fx_weight(float y, float m) {
     return __float2uint_rd(__fmul_rn(fx_exp2_poly(f), scale));
 }
 
+// ---- the same weight for two tokens at once, with packed f32x2 arithmetic (each lane an IEEE fp32
+// operation with round-to-nearest, so the result is bit for bit the scalar fx_weight's)
+__device__ __forceinline__ u64 f2_pack(float lo, float hi) {
+    u64 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(u64 v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ u64 f2_mul(u64 a, u64 b) {
+    u64 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ u64 f2_add(u64 a, u64 b) {
+    u64 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ u64 f2_fma(u64 a, u64 b, u64 c) {
+    u64 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ u64 f2_splat(float x) { return f2_pack(x, x); }
+
+// weights of the tokens with scaled logits y (packed pair) against the row maximum m (negm2 = -m, packed)
+__device__ __forceinline__ void fx_weight2(u64 y2, u64 negm2, uint32_t& w0, uint32_t& w1) {
+    const u64 t2 = f2_mul(f2_add(y2, negm2), f2_splat(0x1.715476p+0f));
+    const u64 r2 = f2_add(t2, f2_splat(12582912.0f));
+    const u64 nf2 = f2_add(r2, f2_splat(-12582912.0f));
+    const u64 f2 = f2_add(t2, nf2 ^ 0x8000000080000000ull);       // t - rint(t)
+    u64 p = f2_splat(0x1.ffcbfcp-17f);
+    p = f2_fma(p, f2, f2_splat(0x1.430912p-13f));
+    p = f2_fma(p, f2, f2_splat(0x1.5d87fep-10f));
+    p = f2_fma(p, f2, f2_splat(0x1.3b2ab6p-7f));
+    p = f2_fma(p, f2, f2_splat(0x1.c6b08ep-5f));
+    p = f2_fma(p, f2, f2_splat(0x1.ebfbe0p-3f));
+    p = f2_fma(p, f2, f2_splat(0x1.62e430p-1f));
+    p = f2_fma(p, f2, f2_splat(1.0f));
+    const int n0 = (int)(uint32_t)r2 - 0x4B400000, n1 = (int)(uint32_t)(r2 >> 32) - 0x4B400000;
+    const u64 sc2 = ((u64)((uint32_t)(127 + 24 + n1) << 23) << 32) | (u64)((uint32_t)(127 + 24 + n0) << 23);
+    float v0, v1, t0, t1;
+    f2_unpack(f2_mul(p, sc2), v0, v1);
+    f2_unpack(t2, t0, t1);
+    w0 = (t0 >= -24.0f) ? __float2uint_rd(v0) : 0u;   // lanes below -24 are discarded whatever they computed
+    w1 = (t1 >= -24.0f) ? __float2uint_rd(v1) : 0u;
+}
+
 // One rejection step of the residual, exactly in integers:
 //   floor(max(0, w * d - wq * X) / d)  =  max(0, w - ceil(wq * X / d)),
 // with X = a * d + b (b < d) and F = floor(2^64 * b / d) prepared once per rejection.  For wq <= 2^25,
@@ -172,17 +222,15 @@ __global__ void __launch_bounds__(kRowThreads) accept_rows_kernel(AcceptArgs a, 
     const float invT = a.invT;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-    float zmax = -INFINITY, ymax = -INFINITY;
+    // y = fp32(z) * invT with invT > 0 is non-decreasing in z, so max y = fp32(max z * invT) and every y is
+    // finite iff every z is and the two extremes stay finite: no per-token multiply in this pass
+    float zmax = -INFINITY, zmin = INFINITY, ymax = -INFINITY;
     int zarg = 0x7fffffff;
     int zfin = 1, yfin = 1;
     auto visit = [&](float z, int k) {
-        zfin &= isfinite(z) ? 1 : 0;
+        zfin &= (fabsf(z) <= 3.402823466e38f) ? 1 : 0;
         if (z > zmax) { zmax = z; zarg = k; }
-        if (STOCH) {
-            float y = __fmul_rn(z, invT);
-            yfin &= isfinite(y) ? 1 : 0;
-            ymax = fmaxf(ymax, y);
-        }
+        if (STOCH) zmin = fminf(zmin, z);
     };
     const bool vec_ok = (V % VEC) == 0;   // every row 16-byte aligned (base checked on the host)
     if (vec_ok) {
@@ -194,6 +242,10 @@ __global__ void __launch_bounds__(kRowThreads) accept_rows_kernel(AcceptArgs a, 
         }
     } else {
         for (int k = c0 + tid; k < c1; k += kRowThreads) visit(LG::load(base + k), k);
+    }
+    if (STOCH) {
+        ymax = __fmul_rn(zmax, invT);
+        yfin = (zmax == -INFINITY || isfinite(ymax)) && (zmin == INFINITY || isfinite(__fmul_rn(zmin, invT)));
     }
     // block combine
 #pragma unroll
@@ -237,11 +289,16 @@ __global__ void __launch_bounds__(kRowThreads) accept_rows_kernel(AcceptArgs a, 
     if (STOCH && tot.fin) {
         const float m = tot.ymax;
         if (vec_ok) {
+            const u64 invT2 = f2_splat(invT), negm2 = f2_splat(-m);
             for (int k = c0 + tid * VEC; k < c1; k += kRowThreads * VEC) {
                 float z[VEC];
                 LG::load_vec(base + k, z);
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) S += fx_weight(__fmul_rn(z[e], invT), m);
+                for (int e = 0; e < VEC; e += 2) {
+                    uint32_t w0, w1;
+                    fx_weight2(f2_mul(f2_pack(z[e], z[e + 1]), invT2), negm2, w0, w1);
+                    S += (u64)w0 + w1;
+                }
             }
         } else {
             for (int k = c0 + tid; k < c1; k += kRowThreads) S += fx_weight(__fmul_rn(LG::load(base + k), invT), m);
@@ -395,12 +452,32 @@ __global__ void __launch_bounds__(kWalkThreads, 2) accept_walk_kernel(AcceptArgs
                 return wres_z(LG::load(prow_p + k), MODE == MODE_PROB ? LG::load(prow_q + k) : 0.f, k);
             };
             // the VEC residual weights of tokens k .. k+VEC-1 (16-byte loads; rows are 16-byte aligned)
+            const u64 invT2 = f2_splat(invT), negmp2 = f2_splat(-sp.ymax);
+            const u64 negmq2 = f2_splat(MODE == MODE_PROB ? -sq.ymax : 0.f);
             auto wres_vec = [&](int k, u64 (&w)[VEC]) {
                 float zp[VEC], zq[VEC];
                 LG::load_vec(prow_p + k, zp);
-                if (MODE == MODE_PROB) LG::load_vec(prow_q + k, zq);
+                if (MODE == MODE_PROB && nrej) LG::load_vec(prow_q + k, zq);
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) w[e] = wres_z(zp[e], MODE == MODE_PROB ? zq[e] : 0.f, k + e);
+                for (int e = 0; e < VEC; e += 2) {
+                    uint32_t p0, p1;
+                    fx_weight2(f2_mul(f2_pack(zp[e], zp[e + 1]), invT2), negmp2, p0, p1);
+                    w[e] = p0;
+                    w[e + 1] = p1;
+                    if (MODE == MODE_ONEHOT) {
+                        for (int i = 0; i < nrej; ++i) {
+                            if ((int)sh.hist[i] == k + e) w[e] = 0;
+                            if ((int)sh.hist[i] == k + e + 1) w[e + 1] = 0;
+                        }
+                    } else if (MODE == MODE_PROB && nrej) {
+                        uint32_t q0, q1;
+                        fx_weight2(f2_mul(f2_pack(zq[e], zq[e + 1]), invT2), negmq2, q0, q1);
+                        for (int i = 0; i < nrej; ++i) {
+                            w[e] = resid_step(w[e], q0, sh.rs[i], Sq);
+                            w[e + 1] = resid_step(w[e + 1], q1, sh.rs[i], Sq);
+                        }
+                    }
+                }
             };
             // Cluster layout of the vocabulary: CTA `rank` owns [k0, k1), its warp w the contiguous segment
             // [s0, s1) (whole vectors when vectorised).  seg_sums() leaves each warp's residual mass in
@@ -564,6 +641,16 @@ __global__ void __launch_bounds__(kWalkThreads, 2) accept_walk_kernel(AcceptArgs
     }
 }
 
+int sm_count() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            n = 1;
+    }
+    return n;
+}
+
 int pick_cluster(int V, int per_cta) {
     int c = (V + per_cta - 1) / per_cta;
     return c < 1 ? 1 : (c > kMaxCluster ? kMaxCluster : c);
@@ -576,7 +663,9 @@ cudaError_t launch_typed(const AcceptArgs& a, cudaStream_t s) {
     const int mode = !stoch ? MODE_GREEDY : (a.draft ? MODE_PROB : MODE_ONEHOT);
     const int rows_src = a.B * a.T;
     const int rows = rows_src * (mode == MODE_PROB ? 2 : 1);
-    const int CL = pick_cluster(a.V, kRowThreads * VEC * 4);
+    // many rows: one CTA per row (no cluster synchronisation); few rows: a cluster splits each row, so the
+    // SMs stay evenly loaded (stochastic rows cost about twice as much, hence the higher bar)
+    const int CL = rows >= (stoch ? 8 : 2) * sm_count() ? 1 : pick_cluster(a.V, kRowThreads * VEC * 4);
     int chunk = (a.V + CL - 1) / CL;
     chunk = (chunk + VEC - 1) / VEC * VEC;
     cudaError_t e;
