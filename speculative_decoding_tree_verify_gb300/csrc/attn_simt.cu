@@ -71,27 +71,47 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(AttnArgs a, float s
     const int npos = L + s_nanc;
 
     for (int start = 0; start < npos; start += kTile) {
-        for (int i = tid; i < kTile * D; i += kThreads) {
-            int r = i / D, d = i - r * D;
-            int j = start + r;
-            float kv = 0.f, vv = 0.f;
-            if (j < npos) {
-                size_t pos = (size_t)(j < L ? j : s_anc[j - L]);
-                kv = KE::get(kp, pos * D + d) * ksc;
-                vv = KE::get(vp, pos * D + d) * vsc;
+        // all loads of a batch are issued before any is used, so a tile costs one memory round trip
+        constexpr int kBatch = 16;
+        for (int base = 0; base < kTile * D; base += kThreads * kBatch) {
+            float kv[kBatch], vv[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int i = base + u * kThreads + tid;
+                const int r = i / D, d = i - r * D;
+                const int j = start + r;
+                kv[u] = 0.f;
+                vv[u] = 0.f;
+                if (i < kTile * D && j < npos) {
+                    const size_t pos = (size_t)(j < L ? j : s_anc[j - L]);
+                    kv[u] = KE::get(kp, pos * D + d);
+                    vv[u] = KE::get(vp, pos * D + d);
+                }
             }
-            ks[r * (D + 1) + d] = kv;
-            vs[r * D + d] = vv;
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int i = base + u * kThreads + tid;
+                if (i < kTile * D) {
+                    const int r = i / D, d = i - r * D;
+                    ks[r * (D + 1) + d] = kv[u] * ksc;
+                    vs[r * D + d] = vv[u] * vsc;
+                }
+            }
         }
         __syncthreads();
         for (int g = warp; g < G; g += kThreads / 32) {
             float s = -INFINITY;
             if (start + lane < npos) {
-                float acc = 0.f;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};   // four independent chains
                 const float* qr = qs + g * D;
                 const float* kr = ks + lane * (D + 1);
-                for (int d = 0; d < D; ++d) acc = fmaf(qr[d], kr[d], acc);
-                s = acc * scale_log2;
+                const int D4 = D & ~3;
+                for (int d = 0; d < D4; d += 4) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) acc[u] = fmaf(qr[d + u], kr[d + u], acc[u]);
+                }
+                for (int d = D4; d < D; ++d) acc[0] = fmaf(qr[d], kr[d], acc[0]);
+                s = ((acc[0] + acc[1]) + (acc[2] + acc[3])) * scale_log2;
             }
             float m_old = ms[g];
             float m_new = fmaxf(m_old, warp_max(s));
@@ -99,9 +119,14 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(AttnArgs a, float s
             float alpha = (m_old == -INFINITY) ? 0.f : exp2f(m_old - m_new);
             float psum = warp_sum(p);
             for (int d = lane; d < D; d += 32) {
-                float acc = os[g * D + d] * alpha;
-                for (int j = 0; j < kTile; ++j) acc = fmaf(__shfl_sync(0xffffffffu, p, j), vs[j * D + d], acc);
-                os[g * D + d] = acc;
+                float acc[4] = {os[g * D + d] * alpha, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int j = 0; j < kTile; j += 4) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        acc[u] = fmaf(__shfl_sync(0xffffffffu, p, j + u), vs[(j + u) * D + d], acc[u]);
+                }
+                os[g * D + d] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
             }
             __syncwarp();
             if (lane == 0) { ls[g] = ls[g] * alpha + psum; ms[g] = m_new; }
