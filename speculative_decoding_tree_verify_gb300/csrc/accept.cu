@@ -234,6 +234,7 @@ __global__ void __launch_bounds__(kRowThreads) accept_rows_kernel(AcceptArgs a, 
     };
     const bool vec_ok = (V % VEC) == 0;   // every row 16-byte aligned (base checked on the host)
     if (vec_ok) {
+#pragma unroll 4
         for (int k = c0 + tid * VEC; k < c1; k += kRowThreads * VEC) {
             float z[VEC];
             LG::load_vec(base + k, z);
@@ -290,6 +291,7 @@ __global__ void __launch_bounds__(kRowThreads) accept_rows_kernel(AcceptArgs a, 
         const float m = tot.ymax;
         if (vec_ok) {
             const u64 invT2 = f2_splat(invT), negm2 = f2_splat(-m);
+#pragma unroll 2
             for (int k = c0 + tid * VEC; k < c1; k += kRowThreads * VEC) {
                 float z[VEC];
                 LG::load_vec(base + k, z);
