@@ -5,7 +5,7 @@
 // the tree be verified in one batched pass).  For one (request b, kv head hk) the T nodes x G query
 // heads form T*G query rows that share every K/V tile, so the contraction is a real GEMM.  Each CTA
 // owns one M tile of 128 query rows:
-//   S = Q K^T  (M = 128 query rows, N = 128 kv positions, K = D = 128)   A = Q from TMEM, B = K
+//   S = Q K^T  (M = 128 query rows, N = 128 kv positions, K = D = 128)   A = Q, B = K, both in shared memory
 //   O += P V   (M = 128 query rows, N = D = 128, K = 128 kv positions)   A = P from TMEM, B = V
 // A "unit" is (request, kv head, group of query rows); it owns ceil((L_b + T) / 128) KV tiles.  When
 // T*G > 128 a unit has 256 rows and is processed by a cluster of two CTAs (one M tile each) that receive
@@ -19,17 +19,19 @@
 // second kernel, attn_merge_kernel, merges them, validates every request and writes the status array.
 //
 // Roles in one CTA of attn_tc_kernel (persistent, 12 warps):
-//   warp 0       TMA producer: K and V tiles (128 x 128 bf16 as two 64-column boxes, 128-byte swizzle)
-//                into a 6-slot ring.
+//   warps 0, 3   TMA producers (bf16 caches): warp 0 loads the K tiles into a 3-slot K ring, warp 3 the V
+//                tiles into a 2-slot V ring (128 x 128 bf16 as two 64-column boxes, 128-byte swizzle), so
+//                K tiles, released as soon as S is computed, run ahead of the V tiles held until the PV.
+//                e4m3 caches: warp 0 loads both into a staging ring and warp 3 converts them to f16.
 //   warp 1       S issuer (also owns the 512 TMEM columns); warp 2 PV issuer.
 //   warps 4-11   softmax: two warps per TMEM lane quadrant, each owning 32 query rows x 64 of the 128
 //                columns of every S tile.  A thread reads its part of an S row, applies the ancestor
 //                mask on the tree block only, keeps a running max (shared with the other half of the
 //                row once per tile) and a partial sum, rescales O lazily when the max grows by > 2^8,
-//                writes P (bf16) to TMEM, and finally normalises its half of the O row and stores it.
-// TMEM holds O, S and four P buffers: S of tile n+1 is computed while the softmax works on tile n (the
-// softmax frees S as soon as the scores are in registers), and the PV of tile n may complete while the
-// softmax works up to three tiles ahead.  Every mbarrier wait is bounded;
+//                writes P to TMEM, and finally normalises its half of the O row and stores it.
+// Q sits in shared memory (the A operand of S = Q K^T); TMEM holds O, two S buffers and two P buffers, so
+// S of tile n+1 is computed while the softmax works on tile n, and the PV of tile n may complete while the
+// softmax writes P of tile n+1.  Every mbarrier wait is bounded;
 // a time-out raises a flag that turns the statuses into SV_ERR_TIMEOUT, and the CTA winds down, waiting
 // (bounded) for its own copies and MMAs before it frees TMEM.
 #include <cuda.h>
@@ -47,31 +49,31 @@ using namespace tc;
 constexpr int kD = 128;
 constexpr int kTileN = 128;                      // kv positions per tile
 constexpr int kRows = 128;                       // query rows per CTA (one M tile)
-constexpr int kRingMax = 6;                      // ring slots (one K or one V tile each): 6 for bf16 KV, 4 for e4m3
+constexpr int kKSlots = 3, kVSlots = 2;          // bf16 KV: a K ring and a V ring (one 32 KB tile per slot)
+constexpr int kRing16 = 3;                       // e4m3 KV: one ring of converted f16 K and V tiles, alternating
 constexpr int kStage8 = 4;                       // e4m3 staging slots (FP8 KV only)
 constexpr int kSlot8Bytes = kTileN * kD;         // 16 KB: one e4m3 K or V tile
 constexpr int kSlotBytes = kTileN * kD * 2;      // 32 KB
 constexpr int kBoxBytes = kSlotBytes / 2;        // one 64-column box: 128 rows x 128 bytes
-constexpr int kThreads = 384;
+constexpr int kThreads = 384;                    // 12 warps
 constexpr int kMaxGrid = 160;                    // the workspace is sized for grids up to this size
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
 constexpr int kMergeThreads = 256;               // 8 warps
 
-constexpr int kSmemRing = 0;                     // bf16 KV: [6][32 KB]; FP8 KV: [4][32 KB] f16 slots, then
+constexpr int kSmemQ = 0;                        // Q of the M tile: [2 halves][16 KB]
+constexpr int kSmemRing = kSlotBytes;            // bf16 KV: [3 K + 2 V][32 KB]; FP8 KV: [3][32 KB] f16 slots, then
 constexpr int kSmemStage = 4 * kSlotBytes;       //   the e4m3 staging slots [4][16 KB]
 constexpr int kSmemBytes = 6 * kSlotBytes;       // 196608 either way
 static_assert(kSmemStage + kStage8 * kSlot8Bytes == kSmemBytes, "FP8 smem layout");
 constexpr int kSmemAlloc = kSmemBytes + 1024;                  // + alignment slack
 
-// TMEM columns (32-bit, one lane per query row): O at 0 (128 columns), S at 128 (128 columns, one buffer:
-// the softmax frees it as soon as it has read the scores), P buffer b at 256 + 64*b (bf16 pairs, kPBufs
-// buffers, so the PV of tile n may finish while the softmax works on tile n+1), Q at 384 (bf16 pairs,
-// 64 columns: the A operand of S = Q K^T).  448 of the 512 columns allocated.
+// TMEM columns (32-bit, one lane per query row): O at 0 (128 columns), S buffer b at 128 + 128*b, P buffer
+// b at 384 + 64*b (bf16 pairs).  S and P are double-buffered: S of tile n+1 is computed while the softmax
+// works on tile n, and the PV of tile n may finish while the softmax writes P of tile n+1.
 constexpr int kPBufs = 2;
 __host__ __device__ constexpr uint32_t col_O() { return 0u; }
-__host__ __device__ constexpr uint32_t col_S() { return 128u; }
-__host__ __device__ constexpr uint32_t col_P(uint32_t b) { return 256u + 64u * b; }
-__host__ __device__ constexpr uint32_t col_Q() { return 384u; }
+__host__ __device__ constexpr uint32_t col_S(uint32_t b) { return 128u + 128u * b; }
+__host__ __device__ constexpr uint32_t col_P(uint32_t b) { return 384u + 64u * b; }
 
 // Workspace: a 256-byte header (time-out flag); per CTA a record of the split unit it completes (if any);
 // two partial-result slots per CTA.  A slot holds O / l in bf16 [128 rows][128], then m (log2 units)
@@ -83,7 +85,7 @@ struct SplitRec {
     int rows;            // valid rows of this CTA's M tile
     int cf;              // first CTA (same cluster rank) holding a segment of the unit
     int cf_slot;         // that CTA's slot for the unit (2 cf, or 2 cf + 1 if it began in an earlier unit)
-    int pad;
+    int err;             // 1: a bounded wait of this CTA gave up (written last, on every launch)
 };
 __host__ __device__ constexpr long long slot_bytes() { return (long long)kRows * kD * 2 + kRows * 8; }
 __host__ __device__ constexpr long long rec_off() { return 256; }
@@ -121,6 +123,24 @@ __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Slot (index into the ring's slots and full/empty barriers) and round of the n-th K (kv = 0) or V (kv = 1)
+// tile a CTA consumes.  bf16 caches: separate K and V rings, so that K tiles, released as soon as S is
+// computed, run ahead of the V tiles, which are held until the PV; e4m3 caches: one ring, K and V alternating.
+template <bool KV8>
+__device__ __forceinline__ void ring_pos(uint32_t n, int kv, uint32_t& slot, uint32_t& round) {
+    if constexpr (KV8) {
+        const uint32_t u = 2 * n + (uint32_t)kv;
+        slot = u % kRing16;
+        round = u / kRing16;
+    } else if (kv == 0) {
+        slot = n % kKSlots;
+        round = n / kKSlots;
+    } else {
+        slot = kKSlots + n % kVSlots;
+        round = n / kVSlots;
+    }
 }
 
 // tiles of one request: its prefix plus its tree block, in 128-position tiles (0 if kv_len is invalid)
@@ -261,15 +281,15 @@ struct SegIter {
 
 // ------------------------------------------------------------------------------------------------ main kernel
 struct MainShared {
-    uint64_t full[kRingMax], empty[kRingMax];
+    uint64_t full[kKSlots + kVSlots], empty[kKSlots + kVSlots];
     uint64_t full8[kStage8], empty8[kStage8];              // e4m3 staging (FP8 KV only)
-    uint64_t s_full, s_free, p_full[kPBufs], pv_done[kPBufs];  // P barriers per P buffer
+    uint64_t s_full[2], s_free[2], p_full[kPBufs], pv_done[kPBufs];   // per S / P buffer
     uint64_t q_full, o_full, drain[2];
+    float xch[2][2][kRows];                                // [tile parity][half][row]: partial row max
+    float lx[2][kRows];                                    // [half][row]: partial row sum
     Plan plan;
     long long scan[33];
     int32_t par[SV_MAX_T];                                 // parent array of the current request
-    float xch[2][2][kRows];                                // [tile parity][half][row]: partial row max
-    float lx[2][kRows];                                    // [half][row]: partial row sum
     uint32_t tmem;
     int err;
 };
@@ -281,12 +301,12 @@ template <int CL, bool KV8>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, AttnArgs a,
                float scale_log2) {
-    constexpr int kStages = KV8 ? 4 : kRingMax;
+    constexpr int kStages = KV8 ? kRing16 : kKSlots + kVSlots;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     __shared__ MainShared sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t sRing = smem_u32(smem + kSmemRing);
+    const uint32_t sQ = smem_u32(smem + kSmemQ), sRing = smem_u32(smem + kSmemRing);
     const int T = a.T, G = a.Hq / a.Hkv, TG = T * G;
     constexpr int kUnitRows = CL * kRows;
     const int QG = (TG + kUnitRows - 1) / kUnitRows, UQ = a.Hkv * QG;
@@ -303,9 +323,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             mbar_init(&sh.full8[i], 1);
             mbar_init(&sh.empty8[i], 1);
         }
-        mbar_init(&sh.s_full, 1);
-        mbar_init(&sh.s_free, 8);                    // one arrival per softmax warp
-        for (int bf = 0; bf < kPBufs; ++bf) {
+        for (int bf = 0; bf < 2; ++bf) {
+            mbar_init(&sh.s_full[bf], 1);
+            mbar_init(&sh.s_free[bf], 8);            // one arrival per softmax warp
             mbar_init(&sh.p_full[bf], 8);
             mbar_init(&sh.pv_done[bf], 1);
         }
@@ -331,33 +351,34 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     volatile int* err = &sh.err;
     const bool active = cid < plan.grid;
 
-    if (warp == 0) {
-        // ---------------------------------------------------------------- TMA producer
+    if (warp == 0 || (!KV8 && warp == 3)) {
+        // ---------------------------------------------------------------- TMA producers
+        // bf16: warp 0 loads the K tiles, warp 3 the V tiles; e4m3: warp 0 loads both into the staging ring
         if (lane == 0 && active) {
-            uint32_t use = 0;
+            const int kv = warp == 0 ? 0 : 1;
+            uint32_t n = 0, use = 0;
             SegIter si;
             si.init(a, plan, UQ, QG);
             Seg sg;
             while (!*err && si.next(sg)) {
                 const int row0 = (sg.b * a.Hkv + sg.hk) * a.kv_cap;
-                for (int t = sg.t0; t < sg.t1 && !*err; ++t) {
+                for (int t = sg.t0; t < sg.t1 && !*err; ++t, ++n) {
                     if constexpr (KV8) {
                         // e4m3 K and V tiles into the staging ring (one 16 KB box each)
-                        for (int kv = 0; kv < 2; ++kv, ++use) {
+                        for (int x = 0; x < 2; ++x, ++use) {
                             const uint32_t slot = use % kStage8, round = use / kStage8;
                             if (!mbar_wait(&sh.empty8[slot], (round & 1) ^ 1, err)) break;
                             mbar_arrive_expect_tx(&sh.full8[slot], kSlot8Bytes);
-                            tma_load_2d(smem + kSmemStage + slot * kSlot8Bytes, kv ? (const void*)&tmV : (const void*)&tmK,
+                            tma_load_2d(smem + kSmemStage + slot * kSlot8Bytes, x ? (const void*)&tmV : (const void*)&tmK,
                                         0, row0 + t * kTileN, &sh.full8[slot]);
                         }
-                        continue;
-                    }
-                    for (int kv = 0; kv < 2; ++kv, ++use) {
-                        const uint32_t slot = use % kStages, round = use / kStages;
+                    } else {
+                        uint32_t slot, round;
+                        ring_pos<KV8>(n, kv, slot, round);
                         // the slot is free in every CTA of the cluster
                         if (!mbar_wait(&sh.empty[slot], (round & 1) ^ 1, err)) break;
                         mbar_arrive_expect_tx(&sh.full[slot], kSlotBytes);
-                        if (CL == 1 || kv == rank) {
+                        if (CL == 1 || kv == rank) {   // in a cluster CTA 0 loads K and CTA 1 loads V, for both
                             uint8_t* dst = smem + kSmemRing + slot * kSlotBytes;
                             const void* tm = kv ? (const void*)&tmV : (const void*)&tmK;
                             if (CL > 1) {
@@ -374,10 +395,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             // wait (bounded) until every CTA of the cluster has released the last slots, so no copy or
             // remote release is still in flight towards this CTA when it exits
             volatile int local = 0;
-            const uint32_t nring = KV8 ? kStage8 : kStages;
-            const uint32_t first_u = use > nring ? use - nring : 0;
-            for (uint32_t u = first_u; u < use && !local; ++u)
-                mbar_wait(KV8 ? &sh.empty8[u % nring] : &sh.empty[u % nring], (u / nring) & 1, &local);
+            if constexpr (KV8) {
+                for (uint32_t u = use > kStage8 ? use - kStage8 : 0; u < use && !local; ++u)
+                    mbar_wait(&sh.empty8[u % kStage8], (u / kStage8) & 1, &local);
+            } else {
+                const uint32_t nslots = kv ? kVSlots : kKSlots;
+                for (uint32_t m = n > nslots ? n - nslots : 0; m < n && !local; ++m) {
+                    uint32_t slot, round;
+                    ring_pos<KV8>(m, kv, slot, round);
+                    mbar_wait(&sh.empty[slot], round & 1, &local);
+                }
+            }
         }
     } else if (warp == 3) {
         // ---------------------------------------------------------------- e4m3 -> f16 converter (FP8 KV)
@@ -427,7 +455,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         // ---------------------------------------------------------------- MMA issuers: S (warp 1), PV (warp 2)
         const bool is_s = warp == 1;
         if (lane == 0 && active) {
-            // A (Q, P) from TMEM; B (K, V) from shared memory; f16 operands for FP8 KV, bf16 otherwise
+            // S: Q and K from shared memory; PV: P from TMEM, V from shared memory; f16 operands for FP8 KV
             const uint32_t idS = KV8 ? idesc_f16_f32(128, kTileN, false, false) : idesc_bf16_f32(128, kTileN, false, false);
             const uint32_t idO = KV8 ? idesc_f16_f32(128, kD, false, true) : idesc_bf16_f32(128, kD, false, true);
             const uint64_t dK = sdesc_sw128(0, 16, 1024);          // K-major operands (Q, K)
@@ -437,7 +465,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 if (CL > 1) mma_commit_mc(&sh.empty[slot], kMask);
                 else mma_commit(&sh.empty[slot]);
             };
-            uint32_t use = 0, gi = 0, nseg = 0;
+            uint32_t gi = 0, nseg = 0;
             bool ok = true;
             SegIter si;
             si.init(a, plan, UQ, QG);
@@ -450,37 +478,38 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 for (int i = 0; i < nt && ok; ++i, ++gi) {
                     const uint32_t b = gi % kPBufs, k = gi / kPBufs;
                     if (is_s) {
-                        const uint32_t u = use + 2 * i;
-                        ok = mbar_wait(&sh.full[u % kStages], (u / kStages) & 1, err);
-                        // the softmax has read the previous tile's scores
-                        if (ok && gi >= 1) ok = mbar_wait(&sh.s_free, (gi - 1) & 1, err);
+                        uint32_t slot, round;
+                        ring_pos<KV8>(gi, 0, slot, round);
+                        ok = mbar_wait(&sh.full[slot], round & 1, err);
+                        // S buffer b was last read by the softmax two tiles ago
+                        if (ok && gi >= 2) ok = mbar_wait(&sh.s_free[b], (k - 1) & 1, err);
                         if (!ok) break;
                         tc_fence_after();
-                        const uint32_t kb = sRing + (u % kStages) * kSlotBytes;
+                        const uint32_t kb = sRing + slot * kSlotBytes;
 #pragma unroll
                         for (int kk = 0; kk < kD / 16; ++kk)
-                            mma_f16_ts(tmem + col_S(), tmem + col_Q() + kk * 8,
+                            mma_f16_ss(tmem + col_S(b), at(dK, sQ + (kk >> 2) * kBoxBytes + (kk & 3) * 32),
                                        at(dK, kb + (kk >> 2) * kBoxBytes + (kk & 3) * 32), idS, kk > 0);
-                        mma_commit(&sh.s_full);
-                        release(u % kStages);
+                        mma_commit(&sh.s_full[b]);
+                        release(slot);
                     } else {
-                        const uint32_t u = use + 2 * i + 1;
-                        ok = mbar_wait(&sh.full[u % kStages], (u / kStages) & 1, err);
+                        uint32_t slot, round;
+                        ring_pos<KV8>(gi, 1, slot, round);
+                        ok = mbar_wait(&sh.full[slot], round & 1, err);
                         if (ok) ok = mbar_wait(&sh.p_full[b], k & 1, err);
                         if (!ok) break;
                         tc_fence_after();
-                        const uint32_t vb = sRing + (u % kStages) * kSlotBytes;
+                        const uint32_t vb = sRing + slot * kSlotBytes;
 #pragma unroll
                         for (int kk = 0; kk < kTileN / 16; ++kk)
                             mma_f16_ts(tmem + col_O(), tmem + col_P(b) + kk * 8, at(dV, vb + kk * 2048), idO,
                                        (i > 0 || kk > 0) ? 1u : 0u);
                         mma_commit(&sh.pv_done[b]);
-                        release(u % kStages);
+                        release(slot);
                     }
                 }
                 if (!ok) break;
                 if (!is_s) mma_commit(&sh.o_full);
-                use += 2 * nt;
                 ++nseg;
             }
             // every MMA this thread issued has completed before TMEM is released
@@ -498,7 +527,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         const int quad = warp & 3;               // TMEM lane quadrant this warp may access
         const int row = quad * 32 + lane;        // query row inside the M tile (= TMEM lane)
         const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
-        uint32_t gi = 0, nseg = 0, use = 0;
+        uint32_t gi = 0, nseg = 0;
         // A warp that hits a time-out stops waiting and touching TMEM but keeps walking the segments, the
         // tiles and every barrier, so no partner is ever left waiting on it.
         bool dead = false;
@@ -515,8 +544,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         while (si.next(sg)) {
             const int b = sg.b, hk = sg.hk;
             const int nt = sg.t1 - sg.t0;
-            const uint32_t use0 = use;
-            use += 2u * nt;
             const int L = __ldg(a.kv_len + b);
             // softmax scale in log2 units (times k_scale for e4m3 K); output scale (v_scale for e4m3 V)
             const float sc = KV8 ? scale_log2 * __ldg(a.k_scale + hk) : scale_log2;
@@ -546,7 +573,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 const int ccf = owner_of(sg.s0, plan.total, plan.grid);
                 r.cf = ccf * CL + rank;
                 r.cf_slot = ((int)((long long)ccf * plan.total / plan.grid) == sg.s0) ? 2 * r.cf : 2 * r.cf + 1;
-                r.pad = 0;
+                r.err = 0;
                 ((SplitRec*)((uint8_t*)a.ws + rec_off()))[blockIdx.x] = r;
             }
             first_seg = false;
@@ -561,28 +588,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 }
             }
             dead = __any_sync(0xffffffffu, dead || *err);
-            // this warp's half (64 of 128 d) of the Q rows -> TMEM, pairs with the even d in the low half (bf16, or
-            // rounded to f16 when the caches are e4m3)
+            // this warp's half (64 of 128 d) of the Q row -> shared memory, box h of the K-major 128-byte-swizzled
+            // A operand of the S MMA (bf16, or rounded to f16 when the caches are e4m3).  The previous segment's
+            // S MMAs have completed: this warp waited for its O before reaching here.
             if (!dead) {
                 const uint4* src = (const uint4*)((const uint16_t*)a.q + out_row * kD) + 8 * h;
-                uint32_t qv[32];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    const uint4 v = valid_row ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-                    qv[4 * c] = v.x;
-                    qv[4 * c + 1] = v.y;
-                    qv[4 * c + 2] = v.z;
-                    qv[4 * c + 3] = v.w;
+                    uint4 v = valid_row ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+                    if constexpr (KV8) {
+                        v.x = pack2<true>(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u));
+                        v.y = pack2<true>(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+                        v.z = pack2<true>(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u));
+                        v.w = pack2<true>(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
+                    }
+                    *(uint4*)(smem + kSmemQ + h * kBoxBytes + sw128_offset(row, c)) = v;
                 }
-                if constexpr (KV8) {
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        qv[c] = pack2<true>(__uint_as_float(qv[c] << 16), __uint_as_float(qv[c] & 0xffff0000u));
-                }
-                __syncwarp();
-                tmem_st32(tmem + lane_addr + col_Q() + 32 * h, qv);
-                tmem_st_wait();
-                tc_fence_before();
+                fence_proxy_async_smem();   // the MMAs (async proxy) read what this thread wrote
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.q_full);
@@ -593,12 +615,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 const int tile0 = (sg.t0 + i) * kTileN;
                 const int pos0 = tile0 + 64 * h;     // position of this warp's first column
                 float s[64];
-                if (wait(&sh.s_full, gi & 1)) {
+                if (wait(&sh.s_full[bb], k & 1)) {
                     tc_fence_after();
                     __syncwarp();
                     uint32_t r0[32], r1[32];
-                    tmem_ld32(tmem + lane_addr + col_S() + 64 * h, r0);
-                    tmem_ld32(tmem + lane_addr + col_S() + 64 * h + 32, r1);
+                    tmem_ld32(tmem + lane_addr + col_S(bb) + 64 * h, r0);
+                    tmem_ld32(tmem + lane_addr + col_S(bb) + 64 * h + 32, r1);
                     tmem_ld_wait();
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
@@ -608,7 +630,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                     // the scores are in registers: the S columns may take the next tile
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&sh.s_free);
+                    if (lane == 0) mbar_arrive(&sh.s_free[bb]);
                 } else {
 #pragma unroll
                     for (int c = 0; c < 64; ++c) s[c] = -INFINITY;
@@ -637,17 +659,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 // the running max m_run straight away; only if some row's max grew by more than 2^8 do the two
                 // warps of the row take the slow path and rewrite the tile's P against the new max.
                 float ps[4], alpha = 1.f, m_use = m_run;
+                // (a row with no finite score has m = -inf and every s = -inf: moff = 0 gives p = 2^-inf = 0)
                 auto exps = [&](float m) {
-                    const bool live = m != -INFINITY;
-                    const float moff = live ? -m * sc : 0.f;
+                    const float moff = m != -INFINITY ? -m * sc : 0.f;
                     ps[0] = ps[1] = ps[2] = ps[3] = 0.f;
 #pragma unroll
                     for (int part2 = 0; part2 < 2; ++part2) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int c = 0; c < 16; ++c) {
-                            const float p0 = live ? ex2(fmaf(s[32 * part2 + 2 * c], sc, moff)) : 0.f;
-                            const float p1 = live ? ex2(fmaf(s[32 * part2 + 2 * c + 1], sc, moff)) : 0.f;
+                            const float p0 = ex2(fmaf(s[32 * part2 + 2 * c], sc, moff));
+                            const float p1 = ex2(fmaf(s[32 * part2 + 2 * c + 1], sc, moff));
                             ps[c & 3] += p0 + p1;
                             pk[c] = pack2<KV8>(p0, p1);
                         }
@@ -695,10 +717,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 // the last tile may hold cache rows past the tree block: zero those V rows in this CTA's copy
                 // of the tile (NaN-safe), fenced before the PV by every writer
                 if (!dead && tile0 + kTileN > L + T) {
-                    const uint32_t vu = use0 + 2u * i + 1u;
-                    if (wait(&sh.full[vu % kStages], (vu / kStages) & 1)) {
+                    uint32_t vslot, vround;
+                    ring_pos<KV8>(gi, 1, vslot, vround);
+                    if (wait(&sh.full[vslot], vround & 1)) {
                         const int r_lo = max(0, L + T - tile0);
-                        uint8_t* vdst = smem + kSmemRing + (vu % kStages) * kSlotBytes;
+                        uint8_t* vdst = smem + kSmemRing + vslot * kSlotBytes;
                         for (int idx = (warp - 4) * 32 + lane; idx < (kTileN - r_lo) * 16; idx += 256) {
                             const int r = r_lo + (idx >> 4), c = idx & 15;
                             *(uint4*)(vdst + (c >> 3) * kBoxBytes + sw128_offset(r, c & 7)) = make_uint4(0, 0, 0, 0);
@@ -771,7 +794,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
-    if (tid == 0 && sh.err) *(volatile int*)a.ws = 1;   // a bounded wait gave up: statuses become TIMEOUT
+    // this CTA's time-out flag (a bounded wait gave up: every status becomes TIMEOUT), written on every launch,
+    // after the record itself
+    if (tid == 0) ((SplitRec*)((uint8_t*)a.ws + rec_off()))[blockIdx.x].err = sh.err;
 }
 
 // ------------------------------------------------------------------------------------------------ merge kernel
@@ -787,7 +812,14 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(AttnArgs a, i
     const int T = a.T, G = a.Hq / a.Hkv;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_wait_prior();   // attention results are visible from here on
-    const bool timeout = *(volatile const int*)a.ws != 0;
+    const SplitRec* recs = (const SplitRec*)((const uint8_t*)a.ws + rec_off());
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+    for (int c = tid; c < grid_main; c += blockDim.x)
+        if (__ldcg(&recs[c].err)) s_bad = 1;
+    __syncthreads();
+    const bool timeout = s_bad != 0;
+    __syncthreads();
 
     // 1. statuses, and zero outputs of failed requests
     for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
@@ -813,7 +845,6 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(AttnArgs a, i
     }
     if (timeout) return;
     // 2. merges
-    const SplitRec* recs = (const SplitRec*)((const uint8_t*)a.ws + rec_off());
     const uint8_t* slots = (const uint8_t*)a.ws + slots_off();
     for (int u = blockIdx.x; u < grid_main * kMergeUnits; u += gridDim.x) {
         const int cl = u / kMergeUnits, rb = u - cl * kMergeUnits;
@@ -981,9 +1012,7 @@ bool attn_tc_supported(const AttnArgs& a) {
 }
 
 cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t s) {
-    // the time-out flag starts clear; the attention kernel only ever sets it
-    cudaError_t e = cudaMemsetAsync(a.ws, 0, 4, s);
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
     const float scale = a.sm_scale != 0.f ? a.sm_scale : (float)(1.0 / sqrt((double)a.D));
     const int CL = cluster_size(a);
     const float sl2 = scale * 1.4426950408889634f;
