@@ -55,7 +55,11 @@ constexpr int kStage8 = 4;                       // e4m3 staging slots (FP8 KV o
 constexpr int kSlot8Bytes = kTileN * kD;         // 16 KB: one e4m3 K or V tile
 constexpr int kSlotBytes = kTileN * kD * 2;      // 32 KB
 constexpr int kBoxBytes = kSlotBytes / 2;        // one 64-column box: 128 rows x 128 bytes
-constexpr int kThreads = 384;                    // 12 warps
+constexpr int kThreads = 384;                    // 12 warps (bf16 caches)
+constexpr int kConv = 4;                         // e4m3 -> f16 converter warps (e4m3 caches): warps 3, 12, 13, 14
+constexpr int kThreads8 = 480;                   // 15 warps (e4m3 caches)
+template <bool KV8>
+constexpr int threads_of() { return KV8 ? kThreads8 : kThreads; }
 constexpr int kMaxGrid = 160;                    // the workspace is sized for grids up to this size
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
 constexpr int kMergeThreads = 256;               // 8 warps
@@ -117,6 +121,27 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
         const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
         return *reinterpret_cast<const uint32_t*>(&h);
     }
+}
+
+// pairs of floats in one 64-bit register pair, and the packed two-lane f32 arithmetic of sm_100+ (each lane
+// rounds exactly as the scalar instruction does)
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -298,7 +323,7 @@ struct MainShared {
 // exactly to f16 (every e4m3 value is an f16 value) into the MMA ring, and the MMAs run on f16 operands
 // (Q and P rounded to f16); k_scale is folded into the softmax scale and v_scale into the epilogue.
 template <int CL, bool KV8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_of<KV8>(), 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, AttnArgs a,
                float scale_log2) {
     constexpr int kStages = KV8 ? kRing16 : kKSlots + kVSlots;
@@ -316,12 +341,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(&sh.full[i], 1);
+            mbar_init(&sh.full[i], KV8 ? kConv : 1);   // the TMA transaction, or one arrival per converter
             mbar_init(&sh.empty[i], CL);             // one release per CTA of the cluster
         }
         for (int i = 0; i < kStage8; ++i) {
             mbar_init(&sh.full8[i], 1);
-            mbar_init(&sh.empty8[i], 1);
+            mbar_init(&sh.empty8[i], kConv);
         }
         for (int bf = 0; bf < 2; ++bf) {
             mbar_init(&sh.s_full[bf], 1);
@@ -407,9 +432,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 }
             }
         }
-    } else if (warp == 3) {
-        // ---------------------------------------------------------------- e4m3 -> f16 converter (FP8 KV)
+    } else if (warp == 3 || warp >= 12) {
+        // ---------------------------------------------------------------- e4m3 -> f16 converters (FP8 KV)
+        // converter ci (warp 3, 12, 13, 14: one per SM sub-partition) converts rows 32 ci .. 32 ci + 31
         if (KV8 && active) {
+            const int ci = warp == 3 ? 0 : warp - 11;
             uint32_t use = 0;
             SegIter si;
             si.init(a, plan, UQ, QG);
@@ -427,7 +454,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                         // chunk j: row j / 8, e4m3 bytes 16 (j % 8) .. +15 -> f16 d 16 (j % 8) .. +15, which is
                         // box (j % 8) / 4, 16-byte chunks 2 (j % 4) and 2 (j % 4) + 1 of that row
 #pragma unroll 4
-                        for (int j = lane; j < kTileN * 8; j += 32) {
+                        for (int j = ci * 256 + lane; j < (ci + 1) * 256; j += 32) {
                             const int r = j >> 3, c = j & 7;
                             const uint4 w = *(const uint4*)(src + r * 128 + c * 16);
                             const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
@@ -554,16 +581,45 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             const int t_node = valid_row ? qi / G : 0, g_head = valid_row ? qi - (qi / G) * G : 0;
             const size_t out_row = ((size_t)b * T + t_node) * a.Hq + (size_t)hk * G + g_head;
             uint8_t* part = sg.split ? (uint8_t*)a.ws + slots_off() + (long long)sg.slot * slot_bytes() : nullptr;
+            dead = __any_sync(0xffffffffu, dead || *err);
+            // first, so that S of the segment's first tile is computed while the ancestors are walked: this warp's
+            // half (64 of 128 d) of the Q row -> shared memory, box h of the K-major 128-byte-swizzled A operand
+            // of the S MMA (bf16, or rounded to f16 when the caches are e4m3).  The previous segment's S MMAs have
+            // completed: this warp waited for its O before reaching here.
+            if (!dead) {
+                const uint4* src = (const uint4*)((const uint16_t*)a.q + out_row * kD) + 8 * h;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 v = valid_row ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+                    if constexpr (KV8) {
+                        v.x = pack2<true>(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u));
+                        v.y = pack2<true>(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+                        v.z = pack2<true>(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u));
+                        v.w = pack2<true>(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
+                    }
+                    *(uint4*)(smem + kSmemQ + h * kBoxBytes + sw128_offset(row, c)) = v;
+                }
+                fence_proxy_async_smem();   // the MMAs (async proxy) read what this thread wrote
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.q_full);
+
             // ancestors of this row's node from the request's parent array (walk bounded by T, so a malformed
             // array cannot trap; such requests are zeroed and flagged by the merge kernel)
             grp_sync();
-            if (h == 0 && row < T) sh.par[row] = __ldg(a.parent + (size_t)b * T + row);
-            grp_sync();
+            int bad = 0;   // this node's parent breaks the tree's topological order
+            if (h == 0 && row < T) {
+                const int px = __ldg(a.parent + (size_t)b * T + row);
+                sh.par[row] = px;
+                bad = row == 0 ? px != -1 : (px < 0 || px >= row);
+            }
+            // the barrier also ORs the flags: bad != 0 everywhere if any node's parent is out of order
+            asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbar.red.or.pred q, 1, 256, p;\n\t"
+                         "selp.s32 %0, 1, 0, q;\n\t}"
+                         : "=r"(bad) : "r"(bad) : "memory");
             if (h == 0 && row == 0 && first_seg) {
                 // the unit that began in an earlier cluster range and ends in this one is merged by
                 // attn_merge_kernel
-                int bad = sh.par[0] != -1;
-                for (int x = 1; x < T; ++x) bad |= sh.par[x] < 0 || sh.par[x] >= x;
                 SplitRec r;
                 r.unit = (sg.s0 < plan.lo && sg.s1 <= plan.hi && !bad) ? sg.unit : -1;
                 r.b = b;
@@ -587,53 +643,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                     x = px;
                 }
             }
-            dead = __any_sync(0xffffffffu, dead || *err);
-            // this warp's half (64 of 128 d) of the Q row -> shared memory, box h of the K-major 128-byte-swizzled
-            // A operand of the S MMA (bf16, or rounded to f16 when the caches are e4m3).  The previous segment's
-            // S MMAs have completed: this warp waited for its O before reaching here.
-            if (!dead) {
-                const uint4* src = (const uint4*)((const uint16_t*)a.q + out_row * kD) + 8 * h;
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint4 v = valid_row ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-                    if constexpr (KV8) {
-                        v.x = pack2<true>(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u));
-                        v.y = pack2<true>(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
-                        v.z = pack2<true>(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u));
-                        v.w = pack2<true>(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
-                    }
-                    *(uint4*)(smem + kSmemQ + h * kBoxBytes + sw128_offset(row, c)) = v;
-                }
-                fence_proxy_async_smem();   // the MMAs (async proxy) read what this thread wrote
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.q_full);
 
             float m_run = -INFINITY, l_run = 0.f;    // running max (raw score units); sum over this half
             for (int i = 0; i < nt; ++i, ++gi) {
                 const uint32_t bb = gi % kPBufs, k = gi / kPBufs;
                 const int tile0 = (sg.t0 + i) * kTileN;
                 const int pos0 = tile0 + 64 * h;     // position of this warp's first column
-                float s[64];
-                if (wait(&sh.s_full[bb], k & 1)) {
-                    tc_fence_after();
-                    __syncwarp();
-                    uint32_t r0[32], r1[32];
-                    tmem_ld32(tmem + lane_addr + col_S(bb) + 64 * h, r0);
-                    tmem_ld32(tmem + lane_addr + col_S(bb) + 64 * h + 32, r1);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        s[c] = __uint_as_float(r0[c]);
-                        s[c + 32] = __uint_as_float(r1[c]);
-                    }
-                    // the scores are in registers: the S columns may take the next tile
+                // this warp's 64 scores of the row, straight from TMEM into the registers the arithmetic uses (a
+                // warp that has timed out still reads, harmlessly, and its results are discarded)
+                const bool have = wait(&sh.s_full[bb], k & 1);
+                tc_fence_after();
+                __syncwarp();
+                uint32_t r0[32], r1[32];
+                tmem_ld32(tmem + lane_addr + col_S(bb) + 64 * h, r0);
+                tmem_ld32(tmem + lane_addr + col_S(bb) + 64 * h + 32, r1);
+                tmem_ld_wait();
+                if (have) {   // the scores are in registers: the S columns may take the tile after next
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&sh.s_free[bb]);
-                } else {
+                }
+                float s[64];
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) s[c] = -INFINITY;
+                for (int c = 0; c < 32; ++c) {
+                    s[c] = __uint_as_float(r0[c]);
+                    s[c + 32] = __uint_as_float(r1[c]);
                 }
                 if (!valid_row) {
 #pragma unroll
@@ -658,24 +692,29 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 // 32 positions at a time.  Fast path (every tile after a row's first): the exponentials use
                 // the running max m_run straight away; only if some row's max grew by more than 2^8 do the two
                 // warps of the row take the slow path and rewrite the tile's P against the new max.
-                float ps[4], alpha = 1.f, m_use = m_run;
+                float ps[4], ps2_hi[4], alpha = 1.f, m_use = m_run;
                 // (a row with no finite score has m = -inf and every s = -inf: moff = 0 gives p = 2^-inf = 0)
+                // (the arguments and the sums two positions at a time, in packed f32x2 arithmetic)
                 auto exps = [&](float m) {
                     const float moff = m != -INFINITY ? -m * sc : 0.f;
-                    ps[0] = ps[1] = ps[2] = ps[3] = 0.f;
+                    const uint64_t sc2 = f2pack(sc, sc), mo2 = f2pack(moff, moff);
+                    uint64_t ps2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                     for (int part2 = 0; part2 < 2; ++part2) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int c = 0; c < 16; ++c) {
-                            const float p0 = ex2(fmaf(s[32 * part2 + 2 * c], sc, moff));
-                            const float p1 = ex2(fmaf(s[32 * part2 + 2 * c + 1], sc, moff));
-                            ps[c & 3] += p0 + p1;
+                            float x0, x1;
+                            f2unpack(f2fma(f2pack(s[32 * part2 + 2 * c], s[32 * part2 + 2 * c + 1]), sc2, mo2), x0, x1);
+                            const float p0 = ex2(x0), p1 = ex2(x1);
+                            ps2[c & 3] = f2add(ps2[c & 3], f2pack(p0, p1));
                             pk[c] = pack2<KV8>(p0, p1);
                         }
                         __syncwarp();
                         if (!dead) tmem_st16(tmem + lane_addr + col_P(bb) + 32 * h + 16 * part2, pk);
                     }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) f2unpack(ps2[j], ps[j], ps2_hi[j]);
                 };
                 bool slow = !__all_sync(0xffffffffu, m_run != -INFINITY || !valid_row);
                 if (!slow) exps(m_run);
@@ -711,7 +750,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                     tmem_st_wait();   // the fast path's P stores land before they are overwritten
                     exps(m_use);
                 }
-                const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+                const float psum = ((ps[0] + ps2_hi[0]) + (ps[1] + ps2_hi[1])) + ((ps[2] + ps2_hi[2]) + (ps[3] + ps2_hi[3]));
                 l_run = (m_run == -INFINITY) ? psum : l_run * alpha + psum;
                 m_run = m_use;
                 // the last tile may hold cache rows past the tree block: zero those V rows in this CTA's copy
@@ -953,7 +992,7 @@ int resident_clusters() {
     if (!n) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(CL * 64);
-        cfg.blockDim = dim3(kThreads);
+        cfg.blockDim = dim3(threads_of<KV8>());
         cfg.dynamicSmemBytes = kSmemAlloc;
         cudaLaunchAttribute attr;
         attr.id = cudaLaunchAttributeClusterDimension;
@@ -983,7 +1022,7 @@ cudaError_t launch_main(const AttnArgs& a, cudaStream_t s, float scale_log2, int
     int ncl = resident_clusters<CL, KV8>();
     if (ncl * CL > kMaxGrid) ncl = kMaxGrid / CL;
     *grid_out = ncl * CL;
-    return launch_ex(attn_tc_kernel<CL, KV8>, dim3(ncl * CL), dim3(kThreads), (size_t)kSmemAlloc, s, CL, false, tmK,
+    return launch_ex(attn_tc_kernel<CL, KV8>, dim3(ncl * CL), dim3(threads_of<KV8>()), (size_t)kSmemAlloc, s, CL, false, tmK,
                      tmV, a, scale_log2);
 }
 
