@@ -665,9 +665,17 @@ cudaError_t launch_typed(const AcceptArgs& a, cudaStream_t s) {
     const int mode = !stoch ? MODE_GREEDY : (a.draft ? MODE_PROB : MODE_ONEHOT);
     const int rows_src = a.B * a.T;
     const int rows = rows_src * (mode == MODE_PROB ? 2 : 1);
-    // many rows: one CTA per row (no cluster synchronisation); few rows: a cluster splits each row, so the
-    // SMs stay evenly loaded (stochastic rows cost about twice as much, hence the higher bar)
-    const int CL = rows >= (stoch ? 8 : 2) * sm_count() ? 1 : pick_cluster(a.V, kRowThreads * VEC * 4);
+    // Stochastic rows: one CTA per row when there are many (no cluster synchronisation), else a cluster
+    // splits each row.  Greedy rows: the largest power-of-two cluster with at most about 9 CTAs per SM in
+    // all, which evens out the last wave (measured on 480 and 192 rows of 128K-152K logits: 2 and 4).
+    int CL;
+    if (stoch) {
+        CL = rows >= 8 * sm_count() ? 1 : pick_cluster(a.V, kRowThreads * VEC * 4);
+    } else {
+        const int cap = pick_cluster(a.V, kRowThreads * VEC * 4);
+        CL = 1;
+        while (CL * 2 <= cap && (long long)rows * CL * 2 <= 9LL * sm_count()) CL *= 2;
+    }
     int chunk = (a.V + CL - 1) / CL;
     chunk = (chunk + VEC - 1) / VEC * VEC;
     cudaError_t e;

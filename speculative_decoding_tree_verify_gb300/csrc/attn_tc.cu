@@ -852,13 +852,18 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(AttnArgs a, i
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_wait_prior();   // attention results are visible from here on
     const SplitRec* recs = (const SplitRec*)((const uint8_t*)a.ws + rec_off());
-    if (tid == 0) s_bad = 0;
-    __syncthreads();
-    for (int c = tid; c < grid_main; c += blockDim.x)
-        if (__ldcg(&recs[c].err)) s_bad = 1;
-    __syncthreads();
-    const bool timeout = s_bad != 0;
-    __syncthreads();
+    // the time-out flags matter only to the CTAs that write statuses: after a time-out every status says so
+    // and the merged outputs (garbage then) are never read
+    bool timeout = false;
+    if (blockIdx.x < a.B) {
+        if (tid == 0) s_bad = 0;
+        __syncthreads();
+        for (int c = tid; c < grid_main; c += blockDim.x)
+            if (__ldcg(&recs[c].err)) s_bad = 1;
+        __syncthreads();
+        timeout = s_bad != 0;
+        __syncthreads();
+    }
 
     // 1. statuses, and zero outputs of failed requests
     for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
@@ -882,7 +887,6 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(AttnArgs a, i
         }
         __syncthreads();
     }
-    if (timeout) return;
     // 2. merges
     const uint8_t* slots = (const uint8_t*)a.ws + slots_off();
     for (int u = blockIdx.x; u < grid_main * kMergeUnits; u += gridDim.x) {
