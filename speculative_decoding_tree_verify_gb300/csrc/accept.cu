@@ -344,6 +344,7 @@ struct WalkShared {
     int32_t par[SV_MAX_T];
     int32_t tok[SV_MAX_T];
     int32_t path[SV_MAX_T];
+    int32_t arg[SV_MAX_T];    // greedy: each row's argmax, gathered once so the walk reads shared memory
     u64 hist[SV_MAX_T];       // PROB: residual sum before each rejection; ONEHOT: rejected tokens
     ResidStep rs[SV_MAX_T];   // PROB: the integer constants of each rejection step
     u64 red[kWalkThreads / 32];
@@ -380,7 +381,9 @@ __global__ void __launch_bounds__(kWalkThreads, 2) accept_walk_kernel(AcceptArgs
     if (st == SV_OK) {
         int nf = 0;
         for (int r = tid; r < T; r += kWalkThreads) {
-            nf |= !stats[(size_t)b * T + r].fin;
+            const RowStat rs = stats[(size_t)b * T + r];
+            nf |= !rs.fin;
+            if (MODE == MODE_GREEDY) sh.arg[r] = rs.arg;
             if (MODE == MODE_PROB) nf |= !stats[(size_t)B * T + (size_t)b * T + r].fin;
         }
         if (__syncthreads_or(nf)) st = SV_ERR_NONFINITE;
@@ -405,7 +408,7 @@ __global__ void __launch_bounds__(kWalkThreads, 2) accept_walk_kernel(AcceptArgs
     if (MODE == MODE_GREEDY) {
         if (writer) {
             for (;;) {
-                int am = stats[(size_t)b * T + cur].arg;
+                const int am = sh.arg[cur];
                 int next = -1;
                 for (int c = cur + 1; c < T; ++c)
                     if (sh.par[c] == cur && sh.tok[c] == am) { next = c; break; }

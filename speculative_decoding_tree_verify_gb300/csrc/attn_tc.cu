@@ -371,6 +371,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     if (CL > 1) cluster_sync_all();   // the peer's barriers are initialised before any multicast reaches them
+    // the merge kernel may be scheduled now: its CTAs take SMs as CTAs of this grid leave them and wait there
+    // (griddepcontrol.wait) until this whole grid has completed
+    pdl_launch_dependents();
     const uint32_t tmem = sh.tmem;
     const Plan& plan = sh.plan;
     volatile int* err = &sh.err;
