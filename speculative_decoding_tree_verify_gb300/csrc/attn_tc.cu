@@ -310,6 +310,8 @@ struct MainShared {
     uint64_t full8[kStage8], empty8[kStage8];              // e4m3 staging (FP8 KV only)
     uint64_t s_full[2], s_free[2], p_full[kPBufs], pv_done[kPBufs];   // per S / P buffer
     uint64_t q_full, o_full, drain[2];
+    uint64_t q_empty;                                      // the segment's S MMAs are done: Q may be replaced
+    uint64_t o_free;                                       // the segment's O has been read by the softmax
     float xch[2][2][kRows];                                // [tile parity][half][row]: partial row max
     float lx[2][kRows];                                    // [half][row]: partial row sum
     Plan plan;
@@ -324,8 +326,8 @@ struct MainShared {
 // (Q and P rounded to f16); k_scale is folded into the softmax scale and v_scale into the epilogue.
 template <int CL, bool KV8>
 __global__ void __launch_bounds__(threads_of<KV8>(), 1)
-attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, AttnArgs a,
-               float scale_log2) {
+attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+               const __grid_constant__ CUtensorMap tmQ, AttnArgs a, float scale_log2, int q_tma) {
     constexpr int kStages = KV8 ? kRing16 : kKSlots + kVSlots;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -356,7 +358,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         }
         mbar_init(&sh.drain[0], 1);
         mbar_init(&sh.drain[1], 1);
-        mbar_init(&sh.q_full, 8);
+        // Q of a segment: loaded by TMA (q_tma: one expect_tx arrival) or written by the eight softmax warps
+        mbar_init(&sh.q_full, q_tma ? 1 : 8);
+        mbar_init(&sh.q_empty, 1);
+        mbar_init(&sh.o_free, 8);
         mbar_init(&sh.o_full, 1);
         sh.err = 0;
         mbar_fence_init();
@@ -384,12 +389,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         // bf16: warp 0 loads the K tiles, warp 3 the V tiles; e4m3: warp 0 loads both into the staging ring
         if (lane == 0 && active) {
             const int kv = warp == 0 ? 0 : 1;
-            uint32_t n = 0, use = 0;
+            uint32_t n = 0, use = 0, nq = 0;
             SegIter si;
             si.init(a, plan, UQ, QG);
             Seg sg;
             while (!*err && si.next(sg)) {
                 const int row0 = (sg.b * a.Hkv + sg.hk) * a.kv_cap;
+                if (!KV8 && q_tma && kv == 0) {
+                    // Q of the segment's M tile (128 query rows = 128/G nodes x G heads) once the previous
+                    // segment's S MMAs no longer read the buffer
+                    if (nq > 0 && !mbar_wait(&sh.q_empty, (nq - 1) & 1, err)) break;
+                    mbar_arrive_expect_tx(&sh.q_full, 2 * kBoxBytes);
+                    const int t0 = (sg.qg * kUnitRows + rank * kRows) / G;
+                    tma_load_3d(smem + kSmemQ, &tmQ, 0, sg.hk * G, sg.b * T + t0, &sh.q_full);
+                    tma_load_3d(smem + kSmemQ + kBoxBytes, &tmQ, 64, sg.hk * G, sg.b * T + t0, &sh.q_full);
+                    ++nq;
+                }
                 for (int t = sg.t0; t < sg.t1 && !*err; ++t, ++n) {
                     if constexpr (KV8) {
                         // e4m3 K and V tiles into the staging ring (one 16 KB box each)
@@ -433,6 +448,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                     ring_pos<KV8>(m, kv, slot, round);
                     mbar_wait(&sh.empty[slot], round & 1, &local);
                 }
+                if (nq > 0 && !local) mbar_wait(&sh.q_full, (nq - 1) & 1, &local);   // the last Q copy has landed
             }
         }
     } else if (warp == 3 || warp >= 12) {
@@ -502,8 +518,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             Seg sg;
             while (ok && !*err && si.next(sg)) {
                 const int nt = sg.t1 - sg.t0;
-                // Q of this segment is in shared memory, and the previous segment's O has been read
-                if (!mbar_wait(&sh.q_full, nseg & 1, err)) break;
+                // S: Q of this segment is in shared memory; PV: the previous segment's O has been read
+                if (is_s ? !mbar_wait(&sh.q_full, nseg & 1, err)
+                         : (nseg > 0 && !mbar_wait(&sh.o_free, (nseg - 1) & 1, err)))
+                    break;
                 tc_fence_after();
                 for (int i = 0; i < nt && ok; ++i, ++gi) {
                     const uint32_t b = gi % kPBufs, k = gi / kPBufs;
@@ -539,7 +557,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                     }
                 }
                 if (!ok) break;
-                if (!is_s) mma_commit(&sh.o_full);
+                if (is_s) mma_commit(&sh.q_empty);   // after the segment's last S MMA
+                else mma_commit(&sh.o_full);
                 ++nseg;
             }
             // every MMA this thread issued has completed before TMEM is released
@@ -585,11 +604,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             const size_t out_row = ((size_t)b * T + t_node) * a.Hq + (size_t)hk * G + g_head;
             uint8_t* part = sg.split ? (uint8_t*)a.ws + slots_off() + (long long)sg.slot * slot_bytes() : nullptr;
             dead = __any_sync(0xffffffffu, dead || *err);
-            // first, so that S of the segment's first tile is computed while the ancestors are walked: this warp's
-            // half (64 of 128 d) of the Q row -> shared memory, box h of the K-major 128-byte-swizzled A operand
-            // of the S MMA (bf16, or rounded to f16 when the caches are e4m3).  The previous segment's S MMAs have
-            // completed: this warp waited for its O before reaching here.
-            if (!dead) {
+            // Q by TMA (the producer), or else first, so that S of the segment's first tile is computed while the
+            // ancestors are walked: this warp's half (64 of 128 d) of the Q row -> shared memory, box h of the
+            // K-major 128-byte-swizzled A operand of the S MMA (bf16, or rounded to f16 when the caches are
+            // e4m3).  The previous segment's S MMAs have completed: this warp waited for its O before reaching here.
+            if (!dead && !q_tma) {
                 const uint4* src = (const uint4*)((const uint16_t*)a.q + out_row * kD) + 8 * h;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
@@ -605,7 +624,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 fence_proxy_async_smem();   // the MMAs (async proxy) read what this thread wrote
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.q_full);
+            if (lane == 0 && !q_tma) mbar_arrive(&sh.q_full);
 
             // ancestors of this row's node from the request's parent array (walk bounded by T, so a malformed
             // array cannot trap; such requests are zeroed and flagged by the merge kernel)
@@ -819,9 +838,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                         a.lse[out_row] = (m_log2 + __log2f(l_tot)) * 0.69314718055994531f;
                     }
                 }
-                // O has been read (the issuers wait for the next segment's q_full before overwriting it)
+                // O has been read: the PV issuer may start the next segment
                 tc_fence_before();
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.o_free);
         }
     }
     if (!active && tid == 0) {   // CTAs beyond the used grid complete no split unit
@@ -991,6 +1012,21 @@ bool encode_kv_map(CUtensorMap* m, const void* base, long long rows, bool e4m3) 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Q as a 3D tensor [B*T][Hq][D] (bf16): a box of 64 d x G heads x 128/G nodes is one 64-column half of an
+// M tile's 128 query rows, landing in shared memory in the row order of the tile (node-major, then head).
+bool encode_q_map(CUtensorMap* m, const AttnArgs& a) {
+    auto enc = tensor_map_encoder();
+    const int G = a.Hq / a.Hkv;
+    if (!enc || G < 1 || kRows % G != 0 || ((uintptr_t)a.q & 15) != 0) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)a.Hq, (cuuint64_t)a.B * a.T};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)a.Hq * kD * 2};
+    cuuint32_t box[3] = {64u, (cuuint32_t)G, (cuuint32_t)(kRows / G)};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Clusters of CL CTAs that fit on the device at once with this kernel's resources (cached per CL); the
 // persistent grid never exceeds it, so every cluster of the grid is resident from the start.
 template <int CL, bool KV8>
@@ -1023,14 +1059,17 @@ cudaError_t launch_main(const AttnArgs& a, cudaStream_t s, float scale_log2, int
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    CUtensorMap tmK, tmV;
+    CUtensorMap tmK, tmV, tmQ;
     const long long rows = (long long)a.B * a.Hkv * a.kv_cap;
     if (!encode_kv_map(&tmK, a.k, rows, KV8) || !encode_kv_map(&tmV, a.v, rows, KV8)) return cudaErrorInvalidValue;
+    // bf16 caches: Q by TMA when the heads of a kv group tile the 128-row M tile; else the softmax writes it
+    const int q_tma = (!KV8 && encode_q_map(&tmQ, a)) ? 1 : 0;
+    if (!q_tma) tmQ = tmK;
     int ncl = resident_clusters<CL, KV8>();
     if (ncl * CL > kMaxGrid) ncl = kMaxGrid / CL;
     *grid_out = ncl * CL;
     return launch_ex(attn_tc_kernel<CL, KV8>, dim3(ncl * CL), dim3(threads_of<KV8>()), (size_t)kSmemAlloc, s, CL, false, tmK,
-                     tmV, a, scale_log2);
+                     tmV, tmQ, a, scale_log2, q_tma);
 }
 
 }  // namespace

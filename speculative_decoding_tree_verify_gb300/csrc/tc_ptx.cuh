@@ -89,6 +89,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int32_t
         : "memory");
 }
 
+// 3D tiled load of one box into shared memory (same rules as the 2D load).
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int32_t x, int32_t y, int32_t z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(smem_u32(dst)), "l"((uint64_t)tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // 2D tiled load of one box, written to the same shared-memory offset in every CTA of the cluster named in
 // cta_mask, each of which receives the complete_tx on its own mbarrier at the offset of `bar`.
 __device__ __forceinline__ void tma_load_2d_mc(void* dst, const void* tmap, int32_t x, int32_t y, uint64_t* bar,
