@@ -56,6 +56,12 @@ SMALL = [
     (2, 1, 8, 1, 128, (1, 1000), "chain", "bf16", "bf16"),
     (2, 20, 4, 2, 64, (31, 33), "star", "f32", "bf16"),
     (2, 7, 6, 3, 96, (50, 90), (2, 2, 1), "bf16", "bf16"),
+    # tensor-core path with Q loaded by the 3D TMA box (G = 1, G = 16 over 2-CTA clusters), and with Q written
+    # by the softmax warps because G does not divide the 128-row M tile (G = 3; G = 6 over 2-CTA clusters)
+    (2, 40, 4, 4, 128, (70, 400), (4, 3, 2), "bf16", "bf16"),
+    (2, 20, 32, 2, 128, (64, 300), (4, 2, 2), "bf16", "bf16"),
+    (2, 11, 9, 3, 128, (90, 400), (3, 2, 2), "bf16", "bf16"),
+    (2, 30, 12, 2, 128, (130, 600), (3, 3, 2, 2), "bf16", "bf16"),
 ]
 
 
