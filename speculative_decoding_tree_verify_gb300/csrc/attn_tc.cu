@@ -671,81 +671,66 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 const uint32_t bb = gi % kPBufs, k = gi / kPBufs;
                 const int tile0 = (sg.t0 + i) * kTileN;
                 const int pos0 = tile0 + 64 * h;     // position of this warp's first column
-                // this warp's 64 scores of the row, straight from TMEM into the registers the arithmetic uses (a
-                // warp that has timed out still reads, harmlessly, and its results are discarded)
+                // this warp's 64 scores of the row, 32 at a time straight from TMEM into the registers the
+                // arithmetic uses (a warp that has timed out still reads, harmlessly, and its results are discarded)
                 const bool have = wait(&sh.s_full[bb], k & 1);
-                tc_fence_after();
-                __syncwarp();
-                uint32_t r0[32], r1[32];
-                tmem_ld32(tmem + lane_addr + col_S(bb) + 64 * h, r0);
-                tmem_ld32(tmem + lane_addr + col_S(bb) + 64 * h + 32, r1);
-                tmem_ld_wait();
-                if (have) {   // the scores are in registers: the S columns may take the tile after next
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&sh.s_free[bb]);
-                }
-                float s[64];
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    s[c] = __uint_as_float(r0[c]);
-                    s[c + 32] = __uint_as_float(r1[c]);
-                }
+                // bit c of allow: column c of this warp's 64 is a prefix position or an ancestor of the row's node
+                // (anc has no bit >= T); padding rows allow nothing
+                uint64_t allow = ~0ull;
                 if (!valid_row) {
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) s[c] = -INFINITY;
+                    allow = 0ull;
                 } else if (pos0 + 64 > L) {   // columns reach the tree block: ancestor mask
-                    // bit c: column c is a prefix position or an ancestor of the row's node (anc has no bit >= T)
                     const int np = L - pos0, a0 = pos0 - L;
                     const uint64_t pre = np >= 64 ? ~0ull : np <= 0 ? 0ull : (1ull << np) - 1ull;
                     const uint64_t tree = a0 >= 64 ? 0ull : a0 >= 0 ? (anc >> a0) : a0 > -64 ? (anc << -a0) : 0ull;
-                    const uint64_t allow = pre | tree;
-                    const uint32_t lo32 = (uint32_t)allow, hi32 = (uint32_t)(allow >> 32);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        if (!((lo32 >> c) & 1u)) s[c] = -INFINITY;
-                        if (!((hi32 >> c) & 1u)) s[c + 32] = -INFINITY;
-                    }
+                    allow = pre | tree;
                 }
                 // P buffer bb was last read by the PV kPBufs tiles ago
                 if (gi >= kPBufs) wait(&sh.pv_done[bb], (k - 1) & 1);
                 tc_fence_after();
-                // P = 2^(s*scale - m) in bf16, packed in pairs (even k in the low half), into P buffer bb,
-                // 32 positions at a time.  Fast path (every tile after a row's first): the exponentials use
-                // the running max m_run straight away; only if some row's max grew by more than 2^8 do the two
-                // warps of the row take the slow path and rewrite the tile's P against the new max.
-                float ps[4], ps2_hi[4], alpha = 1.f, m_use = m_run;
-                // (a row with no finite score has m = -inf and every s = -inf: moff = 0 gives p = 2^-inf = 0)
-                // (the arguments and the sums two positions at a time, in packed f32x2 arithmetic)
-                auto exps = [&](float m) {
+                __syncwarp();
+                // P = 2^(s*scale - m) in bf16, packed in pairs (even position in the low half), into P buffer bb.
+                // Fast path (every tile after a row's first): the exponentials use the running max m_run straight
+                // away; only if some row's max grew by more than 2^8 do the two warps of the row take the slow path
+                // and rewrite the tile's P against the new max, reading the scores again (S is freed only then).
+                // (a row with no finite score has m = -inf and every s = -inf: moff = 0 gives p = 2^-inf = 0;
+                // the arguments and the sums run two positions at a time, in packed f32x2 arithmetic)
+                uint64_t ps2[4];
+                float tmax_h = -INFINITY;
+                auto chunk = [&](int ch, float m, bool do_exp) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_addr + col_S(bb) + 64 * h + 32 * ch, r);
+                    tmem_ld_wait();
+                    const uint32_t al = (uint32_t)(allow >> (32 * ch));
+                    float s[32];
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) s[c] = ((al >> c) & 1u) ? __uint_as_float(r[c]) : -INFINITY;
+                    float mx[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        mx[c] = max3(max3(s[c], s[c + 4], s[c + 8]), max3(s[c + 12], s[c + 16], s[c + 20]),
+                                     fmaxf(s[c + 24], s[c + 28]));
+                    tmax_h = max3(tmax_h, max3(mx[0], mx[1], mx[2]), mx[3]);
+                    if (!do_exp) return;
                     const float moff = m != -INFINITY ? -m * sc : 0.f;
                     const uint64_t sc2 = f2pack(sc, sc), mo2 = f2pack(moff, moff);
-                    uint64_t ps2[4] = {0ull, 0ull, 0ull, 0ull};
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int part2 = 0; part2 < 2; ++part2) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            float x0, x1;
-                            f2unpack(f2fma(f2pack(s[32 * part2 + 2 * c], s[32 * part2 + 2 * c + 1]), sc2, mo2), x0, x1);
-                            const float p0 = ex2(x0), p1 = ex2(x1);
-                            ps2[c & 3] = f2add(ps2[c & 3], f2pack(p0, p1));
-                            pk[c] = pack2<KV8>(p0, p1);
-                        }
-                        __syncwarp();
-                        if (!dead) tmem_st16(tmem + lane_addr + col_P(bb) + 32 * h + 16 * part2, pk);
+                    for (int c = 0; c < 16; ++c) {
+                        float x0, x1;
+                        f2unpack(f2fma(f2pack(s[2 * c], s[2 * c + 1]), sc2, mo2), x0, x1);
+                        const float p0 = ex2(x0), p1 = ex2(x1);
+                        ps2[c & 3] = f2add(ps2[c & 3], f2pack(p0, p1));
+                        pk[c] = pack2<KV8>(p0, p1);
                     }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) f2unpack(ps2[j], ps[j], ps2_hi[j]);
+                    __syncwarp();
+                    if (!dead) tmem_st16(tmem + lane_addr + col_P(bb) + 32 * h + 16 * ch, pk);
                 };
+                float alpha = 1.f, m_use = m_run;
                 bool slow = !__all_sync(0xffffffffu, m_run != -INFINITY || !valid_row);
-                if (!slow) exps(m_run);
-                float mx[8];
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    mx[c] = max3(max3(s[c], s[c + 8], s[c + 16]), max3(s[c + 24], s[c + 32], s[c + 40]),
-                                 fmaxf(s[c + 48], s[c + 56]));
-                const float tmax_h = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+                ps2[0] = ps2[1] = ps2[2] = ps2[3] = 0ull;
+#pragma unroll 1
+                for (int ch = 0; ch < 2; ++ch) chunk(ch, m_run, !slow);
                 sh.xch[gi & 1][h][row] = tmax_h;   // double-buffered by tile parity: one barrier per tile
                 pair_sync();
                 const float tmax = fmaxf(tmax_h, sh.xch[gi & 1][h ^ 1][row]);
@@ -758,7 +743,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                     // O holds PV of the previous tile: wait for it, then rescale this warp's half of O
                     if (__any_sync(0xffffffffu, rescale) && wait(&sh.pv_done[(gi - 1) % kPBufs], ((gi - 1) / kPBufs) & 1)) {
                         tc_fence_after();
-                        for (int c = 0; c < 4; ++c) {   // 16 columns at a time: the scores stay in registers
+                        for (int c = 0; c < 4; ++c) {   // 16 columns at a time
                             uint32_t o[16];
                             __syncwarp();
                             tmem_ld16(tmem + lane_addr + col_O() + 64 * h + 16 * c, o);
@@ -770,8 +755,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                         tmem_st_wait();
                     }
                     tmem_st_wait();   // the fast path's P stores land before they are overwritten
-                    exps(m_use);
+                    ps2[0] = ps2[1] = ps2[2] = ps2[3] = 0ull;
+#pragma unroll 1
+                    for (int ch = 0; ch < 2; ++ch) chunk(ch, m_use, true);
                 }
+                if (have) {   // the scores have been read for the last time: S may take the tile after next
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sh.s_free[bb]);
+                }
+                float ps[4], ps2_hi[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) f2unpack(ps2[j], ps[j], ps2_hi[j]);
                 const float psum = ((ps[0] + ps2_hi[0]) + (ps[1] + ps2_hi[1])) + ((ps[2] + ps2_hi[2]) + (ps[3] + ps2_hi[3]));
                 l_run = (m_run == -INFINITY) ? psum : l_run * alpha + psum;
                 m_run = m_use;
