@@ -55,7 +55,8 @@ constexpr int kStage8 = 4;                       // e4m3 staging slots (FP8 KV o
 constexpr int kSlot8Bytes = kTileN * kD;         // 16 KB: one e4m3 K or V tile
 constexpr int kSlotBytes = kTileN * kD * 2;      // 32 KB
 constexpr int kBoxBytes = kSlotBytes / 2;        // one 64-column box: 128 rows x 128 bytes
-constexpr int kThreads = 384;                    // 12 warps (bf16 caches)
+constexpr int kSplit16 = 2;                      // bf16 caches: softmax warps per query row (4 measured slower)
+constexpr int kThreads = 128 + 128 * kSplit16;   // 4 role warps + 4 * kSplit16 softmax warps (bf16 caches)
 constexpr int kConv = 4;                         // e4m3 -> f16 converter warps (e4m3 caches): warps 3, 12, 13, 14
 constexpr int kThreads8 = 480;                   // 15 warps (e4m3 caches)
 template <bool KV8>
@@ -312,8 +313,8 @@ struct MainShared {
     uint64_t q_full, o_full, drain[2];
     uint64_t q_empty;                                      // the segment's S MMAs are done: Q may be replaced
     uint64_t o_free;                                       // the segment's O has been read by the softmax
-    float xch[2][2][kRows];                                // [tile parity][half][row]: partial row max
-    float lx[2][kRows];                                    // [half][row]: partial row sum
+    float xch[2][4][kRows];                                // [tile parity][column part][row]: partial row max
+    float lx[4][kRows];                                    // [column part][row]: partial row sum
     Plan plan;
     long long scan[33];
     int32_t par[SV_MAX_T];                                 // parent array of the current request
@@ -329,6 +330,8 @@ __global__ void __launch_bounds__(threads_of<KV8>(), 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const __grid_constant__ CUtensorMap tmQ, AttnArgs a, float scale_log2, int q_tma) {
     constexpr int kStages = KV8 ? kRing16 : kKSlots + kVSlots;
+    constexpr int SPL = KV8 ? 2 : kSplit16;          // softmax warps per query row
+    constexpr int COLS = kTileN / SPL;               // S columns (and O columns in the epilogue) per softmax warp
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     __shared__ MainShared sh;
@@ -352,16 +355,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         }
         for (int bf = 0; bf < 2; ++bf) {
             mbar_init(&sh.s_full[bf], 1);
-            mbar_init(&sh.s_free[bf], 8);            // one arrival per softmax warp
-            mbar_init(&sh.p_full[bf], 8);
+            mbar_init(&sh.s_free[bf], 4 * SPL);      // one arrival per softmax warp
+            mbar_init(&sh.p_full[bf], 4 * SPL);
             mbar_init(&sh.pv_done[bf], 1);
         }
         mbar_init(&sh.drain[0], 1);
         mbar_init(&sh.drain[1], 1);
         // Q of a segment: loaded by TMA (q_tma: one expect_tx arrival) or written by the eight softmax warps
-        mbar_init(&sh.q_full, q_tma ? 1 : 8);
+        mbar_init(&sh.q_full, q_tma ? 1 : 4 * SPL);
         mbar_init(&sh.q_empty, 1);
-        mbar_init(&sh.o_free, 8);
+        mbar_init(&sh.o_free, 4 * SPL);
         mbar_init(&sh.o_full, 1);
         sh.err = 0;
         mbar_fence_init();
@@ -451,7 +454,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 if (nq > 0 && !local) mbar_wait(&sh.q_full, (nq - 1) & 1, &local);   // the last Q copy has landed
             }
         }
-    } else if (warp == 3 || warp >= 12) {
+    } else if (KV8 && (warp == 3 || warp >= 12)) {
         // ---------------------------------------------------------------- e4m3 -> f16 converters (FP8 KV)
         // converter ci (warp 3, 12, 13, 14: one per SM sub-partition) converts rows 32 ci .. 32 ci + 31
         if (KV8 && active) {
@@ -572,7 +575,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         // Warp 4 + 4h + i owns TMEM lane quadrant q = warp % 4 (query rows 32q .. 32q+31) and columns
         // [64h, 64h + 64) of every S tile.  The two warps that share a quadrant (h = 0, 1) agree on the row
         // max through shared memory once per tile, and split the d columns of the epilogue.
-        const int h = (warp - 4) >> 2;           // column half
+        const int h = (warp - 4) >> 2;           // column part
         const int quad = warp & 3;               // TMEM lane quadrant this warp may access
         const int row = quad * 32 + lane;        // query row inside the M tile (= TMEM lane)
         const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
@@ -584,8 +587,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             if (!dead) dead = __any_sync(0xffffffffu, !mbar_wait(bar, parity, err));
             return !dead;
         };
-        auto grp_sync = [&]() { asm volatile("bar.sync 1, 256;" ::: "memory"); };
-        auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(2 + quad) : "memory"); };
+        auto grp_sync = [&]() { asm volatile("bar.sync 1, %0;" ::"n"(128 * SPL) : "memory"); };
+        auto pair_sync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(2 + quad), "n"(32 * SPL) : "memory"); };
         SegIter si;
         si.init(a, plan, UQ, QG);
         Seg sg;
@@ -609,9 +612,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             // K-major 128-byte-swizzled A operand of the S MMA (bf16, or rounded to f16 when the caches are
             // e4m3).  The previous segment's S MMAs have completed: this warp waited for its O before reaching here.
             if (!dead && !q_tma) {
-                const uint4* src = (const uint4*)((const uint16_t*)a.q + out_row * kD) + 8 * h;
+                const uint4* src = (const uint4*)((const uint16_t*)a.q + out_row * kD) + (COLS / 8) * h;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
+                for (int c = 0; c < COLS / 8; ++c) {
                     uint4 v = valid_row ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
                     if constexpr (KV8) {
                         v.x = pack2<true>(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u));
@@ -619,7 +622,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                         v.z = pack2<true>(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u));
                         v.w = pack2<true>(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
                     }
-                    *(uint4*)(smem + kSmemQ + h * kBoxBytes + sw128_offset(row, c)) = v;
+                    const int d8 = h * (COLS / 8) + c;   // 16-byte chunk of the row: box d8 / 8, chunk d8 % 8
+                    *(uint4*)(smem + kSmemQ + (d8 >> 3) * kBoxBytes + sw128_offset(row, d8 & 7)) = v;
                 }
                 fence_proxy_async_smem();   // the MMAs (async proxy) read what this thread wrote
             }
@@ -636,9 +640,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 bad = row == 0 ? px != -1 : (px < 0 || px >= row);
             }
             // the barrier also ORs the flags: bad != 0 everywhere if any node's parent is out of order
-            asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbar.red.or.pred q, 1, 256, p;\n\t"
+            asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbar.red.or.pred q, 1, %2, p;\n\t"
                          "selp.s32 %0, 1, 0, q;\n\t}"
-                         : "=r"(bad) : "r"(bad) : "memory");
+                         : "=r"(bad) : "r"(bad), "n"(128 * SPL) : "memory");
             if (h == 0 && row == 0 && first_seg) {
                 // the unit that began in an earlier cluster range and ends in this one is merged by
                 // attn_merge_kernel
@@ -670,7 +674,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             for (int i = 0; i < nt; ++i, ++gi) {
                 const uint32_t bb = gi % kPBufs, k = gi / kPBufs;
                 const int tile0 = (sg.t0 + i) * kTileN;
-                const int pos0 = tile0 + 64 * h;     // position of this warp's first column
+                const int pos0 = tile0 + COLS * h;   // position of this warp's first column
                 // this warp's 64 scores of the row, 32 at a time straight from TMEM into the registers the
                 // arithmetic uses (a warp that has timed out still reads, harmlessly, and its results are discarded)
                 const bool have = wait(&sh.s_full[bb], k & 1);
@@ -679,7 +683,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 uint64_t allow = ~0ull;
                 if (!valid_row) {
                     allow = 0ull;
-                } else if (pos0 + 64 > L) {   // columns reach the tree block: ancestor mask
+                } else if (pos0 + COLS > L) {   // columns reach the tree block: ancestor mask
                     const int np = L - pos0, a0 = pos0 - L;
                     const uint64_t pre = np >= 64 ? ~0ull : np <= 0 ? 0ull : (1ull << np) - 1ull;
                     const uint64_t tree = a0 >= 64 ? 0ull : a0 >= 0 ? (anc >> a0) : a0 > -64 ? (anc << -a0) : 0ull;
@@ -699,7 +703,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 float tmax_h = -INFINITY;
                 auto chunk = [&](int ch, float m, bool do_exp) {
                     uint32_t r[32];
-                    tmem_ld32(tmem + lane_addr + col_S(bb) + 64 * h + 32 * ch, r);
+                    tmem_ld32(tmem + lane_addr + col_S(bb) + COLS * h + 32 * ch, r);
                     tmem_ld_wait();
                     const uint32_t al = (uint32_t)(allow >> (32 * ch));
                     float s[32];
@@ -724,16 +728,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                         pk[c] = pack2<KV8>(p0, p1);
                     }
                     __syncwarp();
-                    if (!dead) tmem_st16(tmem + lane_addr + col_P(bb) + 32 * h + 16 * ch, pk);
+                    if (!dead) tmem_st16(tmem + lane_addr + col_P(bb) + (COLS / 2) * h + 16 * ch, pk);
                 };
                 float alpha = 1.f, m_use = m_run;
                 bool slow = !__all_sync(0xffffffffu, m_run != -INFINITY || !valid_row);
                 ps2[0] = ps2[1] = ps2[2] = ps2[3] = 0ull;
 #pragma unroll 1
-                for (int ch = 0; ch < 2; ++ch) chunk(ch, m_run, !slow);
+                for (int ch = 0; ch < COLS / 32; ++ch) chunk(ch, m_run, !slow);
                 sh.xch[gi & 1][h][row] = tmax_h;   // double-buffered by tile parity: one barrier per tile
                 pair_sync();
-                const float tmax = fmaxf(tmax_h, sh.xch[gi & 1][h ^ 1][row]);
+                float tmax = tmax_h;
+#pragma unroll
+                for (int j = 0; j < SPL; ++j) tmax = fmaxf(tmax, sh.xch[gi & 1][j][row]);
                 if (!slow) slow = __any_sync(0xffffffffu, valid_row && (tmax - m_run) * sc > kRescaleThreshold);
                 if (slow) {
                     const float m_new = fmaxf(m_run, tmax);
@@ -743,21 +749,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                     // O holds PV of the previous tile: wait for it, then rescale this warp's half of O
                     if (__any_sync(0xffffffffu, rescale) && wait(&sh.pv_done[(gi - 1) % kPBufs], ((gi - 1) / kPBufs) & 1)) {
                         tc_fence_after();
-                        for (int c = 0; c < 4; ++c) {   // 16 columns at a time
+                        for (int c = 0; c < COLS / 16; ++c) {   // 16 columns at a time
                             uint32_t o[16];
                             __syncwarp();
-                            tmem_ld16(tmem + lane_addr + col_O() + 64 * h + 16 * c, o);
+                            tmem_ld16(tmem + lane_addr + col_O() + COLS * h + 16 * c, o);
                             tmem_ld_wait();
 #pragma unroll
                             for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                            tmem_st16(tmem + lane_addr + col_O() + 64 * h + 16 * c, o);
+                            tmem_st16(tmem + lane_addr + col_O() + COLS * h + 16 * c, o);
                         }
                         tmem_st_wait();
                     }
                     tmem_st_wait();   // the fast path's P stores land before they are overwritten
                     ps2[0] = ps2[1] = ps2[2] = ps2[3] = 0ull;
 #pragma unroll 1
-                    for (int ch = 0; ch < 2; ++ch) chunk(ch, m_use, true);
+                    for (int ch = 0; ch < COLS / 32; ++ch) chunk(ch, m_use, true);
                 }
                 if (have) {   // the scores have been read for the last time: S may take the tile after next
                     tc_fence_before();
@@ -778,7 +784,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                     if (wait(&sh.full[vslot], vround & 1)) {
                         const int r_lo = max(0, L + T - tile0);
                         uint8_t* vdst = smem + kSmemRing + vslot * kSlotBytes;
-                        for (int idx = (warp - 4) * 32 + lane; idx < (kTileN - r_lo) * 16; idx += 256) {
+                        for (int idx = (warp - 4) * 32 + lane; idx < (kTileN - r_lo) * 16; idx += 128 * SPL) {
                             const int r = r_lo + (idx >> 4), c = idx & 15;
                             *(uint4*)(vdst + (c >> 3) * kBoxBytes + sw128_offset(r, c & 7)) = make_uint4(0, 0, 0, 0);
                         }
@@ -795,19 +801,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             // epilogue: all MMAs of the segment are complete
             if (wait(&sh.o_full, nseg & 1)) tc_fence_after();
             ++nseg;
-            sh.lx[h][row] = l_run;                    // the row's sum is split between the two halves
+            sh.lx[h][row] = l_run;                    // the row's sum is split between the row's warps
             pair_sync();
-            const float l_tot = l_run + sh.lx[h ^ 1][row];
+            float l_tot = 0.f;
+#pragma unroll
+            for (int j = 0; j < SPL; ++j) l_tot += sh.lx[j][row];
             if (!dead) {
                 const float m_log2 = m_run * sc;
-                // normalised O (bf16, this warp's 64 d columns) either to the output row or to the partial slot
+                // normalised O (bf16, this warp's COLS d columns) either to the output row or to the partial slot
                 const float inv_l = l_tot > 0.f ? osc / l_tot : 0.f;
-                uint16_t* dst_row = (part ? (uint16_t*)part + (size_t)row * kD : (uint16_t*)a.out + out_row * kD) + 64 * h;
+                uint16_t* dst_row = (part ? (uint16_t*)part + (size_t)row * kD : (uint16_t*)a.out + out_row * kD) + COLS * h;
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < COLS / 32; ++c) {
                     uint32_t o[32];
                     __syncwarp();
-                    tmem_ld32(tmem + lane_addr + col_O() + 64 * h + 32 * c, o);
+                    tmem_ld32(tmem + lane_addr + col_O() + COLS * h + 32 * c, o);
                     tmem_ld_wait();
                     if (valid_row) {
                         uint4* dst = (uint4*)(dst_row + c * 32);
