@@ -49,7 +49,7 @@ using namespace tc;
 constexpr int kD = 128;
 constexpr int kTileN = 128;                      // kv positions per tile
 constexpr int kRows = 128;                       // query rows per CTA (one M tile)
-constexpr int kKSlots = 3, kVSlots = 2;          // bf16 KV: a K ring and a V ring (one 32 KB tile per slot)
+constexpr int kKSlots = 2, kVSlots = 2;          // bf16 KV: a K ring and a V ring (one 32 KB tile per slot)
 constexpr int kRing16 = 3;                       // e4m3 KV: one ring of converted f16 K and V tiles, alternating
 constexpr int kStage8 = 4;                       // e4m3 staging slots (FP8 KV only)
 constexpr int kSlot8Bytes = kTileN * kD;         // 16 KB: one e4m3 K or V tile
@@ -65,8 +65,10 @@ constexpr int kMaxGrid = 160;                    // the workspace is sized for g
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
 constexpr int kMergeThreads = 256;               // 8 warps
 
-constexpr int kSmemQ = 0;                        // Q of the M tile: [2 halves][16 KB]
-constexpr int kSmemRing = kSlotBytes;            // bf16 KV: [3 K + 2 V][32 KB]; FP8 KV: [3][32 KB] f16 slots, then
+constexpr int kSmemQ = 0;                        // Q of the M tile: [buffer][2 halves][16 KB] (2 buffers for bf16)
+// ring: bf16 KV: [2 K + 2 V][32 KB] after two Q buffers; FP8 KV: [3][32 KB] f16 slots after one Q buffer, then
+template <bool KV8>
+__host__ __device__ constexpr int ring_off() { return KV8 ? kSlotBytes : 2 * kSlotBytes; }
 constexpr int kSmemStage = 4 * kSlotBytes;       //   the e4m3 staging slots [4][16 KB]
 constexpr int kSmemBytes = 6 * kSlotBytes;       // 196608 either way
 static_assert(kSmemStage + kStage8 * kSlot8Bytes == kSmemBytes, "FP8 smem layout");
@@ -310,8 +312,8 @@ struct MainShared {
     uint64_t full[kKSlots + kVSlots], empty[kKSlots + kVSlots];
     uint64_t full8[kStage8], empty8[kStage8];              // e4m3 staging (FP8 KV only)
     uint64_t s_full[2], s_free[2], p_full[kPBufs], pv_done[kPBufs];   // per S / P buffer
-    uint64_t q_full, o_full, drain[2];
-    uint64_t q_empty;                                      // the segment's S MMAs are done: Q may be replaced
+    uint64_t q_full[2], o_full, drain[2];                  // per Q buffer
+    uint64_t q_empty[2];                                   // per Q buffer: its segment's S MMAs are done
     uint64_t o_free;                                       // the segment's O has been read by the softmax
     float xch[2][4][kRows];                                // [tile parity][column part][row]: partial row max
     float lx[4][kRows];                                    // [column part][row]: partial row sum
@@ -330,6 +332,8 @@ __global__ void __launch_bounds__(threads_of<KV8>(), 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const __grid_constant__ CUtensorMap tmQ, AttnArgs a, float scale_log2, int q_tma) {
     constexpr int kStages = KV8 ? kRing16 : kKSlots + kVSlots;
+    constexpr int QB = KV8 ? 1 : 2;                  // Q buffers: segment s uses buffer s % QB
+    constexpr int kSmemRing = ring_off<KV8>();
     constexpr int SPL = KV8 ? 2 : kSplit16;          // softmax warps per query row
     constexpr int COLS = kTileN / SPL;               // S columns (and O columns in the epilogue) per softmax warp
     extern __shared__ uint8_t smem_raw[];
@@ -362,8 +366,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         mbar_init(&sh.drain[0], 1);
         mbar_init(&sh.drain[1], 1);
         // Q of a segment: loaded by TMA (q_tma: one expect_tx arrival) or written by the eight softmax warps
-        mbar_init(&sh.q_full, q_tma ? 1 : 4 * SPL);
-        mbar_init(&sh.q_empty, 1);
+        for (int qb = 0; qb < 2; ++qb) {
+            mbar_init(&sh.q_full[qb], q_tma ? 1 : 4 * SPL);
+            mbar_init(&sh.q_empty[qb], 1);
+        }
         mbar_init(&sh.o_free, 4 * SPL);
         mbar_init(&sh.o_full, 1);
         sh.err = 0;
@@ -401,11 +407,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 if (!KV8 && q_tma && kv == 0) {
                     // Q of the segment's M tile (128 query rows = 128/G nodes x G heads) once the previous
                     // segment's S MMAs no longer read the buffer
-                    if (nq > 0 && !mbar_wait(&sh.q_empty, (nq - 1) & 1, err)) break;
-                    mbar_arrive_expect_tx(&sh.q_full, 2 * kBoxBytes);
+                    const uint32_t qb = nq % QB;
+                    if (nq >= (uint32_t)QB && !mbar_wait(&sh.q_empty[qb], (nq / QB - 1) & 1, err)) break;
+                    mbar_arrive_expect_tx(&sh.q_full[qb], 2 * kBoxBytes);
                     const int t0 = (sg.qg * kUnitRows + rank * kRows) / G;
-                    tma_load_3d(smem + kSmemQ, &tmQ, 0, sg.hk * G, sg.b * T + t0, &sh.q_full);
-                    tma_load_3d(smem + kSmemQ + kBoxBytes, &tmQ, 64, sg.hk * G, sg.b * T + t0, &sh.q_full);
+                    uint8_t* qdst = smem + kSmemQ + qb * kSlotBytes;
+                    tma_load_3d(qdst, &tmQ, 0, sg.hk * G, sg.b * T + t0, &sh.q_full[qb]);
+                    tma_load_3d(qdst + kBoxBytes, &tmQ, 64, sg.hk * G, sg.b * T + t0, &sh.q_full[qb]);
                     ++nq;
                 }
                 for (int t = sg.t0; t < sg.t1 && !*err; ++t, ++n) {
@@ -451,7 +459,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                     ring_pos<KV8>(m, kv, slot, round);
                     mbar_wait(&sh.empty[slot], round & 1, &local);
                 }
-                if (nq > 0 && !local) mbar_wait(&sh.q_full, (nq - 1) & 1, &local);   // the last Q copy has landed
+                if (nq > 0 && !local)   // the last Q copy has landed
+                    mbar_wait(&sh.q_full[(nq - 1) % QB], ((nq - 1) / QB) & 1, &local);
             }
         }
     } else if (KV8 && (warp == 3 || warp >= 12)) {
@@ -522,7 +531,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             while (ok && !*err && si.next(sg)) {
                 const int nt = sg.t1 - sg.t0;
                 // S: Q of this segment is in shared memory; PV: the previous segment's O has been read
-                if (is_s ? !mbar_wait(&sh.q_full, nseg & 1, err)
+                const uint32_t qb = nseg % QB;
+                if (is_s ? !mbar_wait(&sh.q_full[qb], (nseg / QB) & 1, err)
                          : (nseg > 0 && !mbar_wait(&sh.o_free, (nseg - 1) & 1, err)))
                     break;
                 tc_fence_after();
@@ -539,7 +549,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                         const uint32_t kb = sRing + slot * kSlotBytes;
 #pragma unroll
                         for (int kk = 0; kk < kD / 16; ++kk)
-                            mma_f16_ss(tmem + col_S(b), at(dK, sQ + (kk >> 2) * kBoxBytes + (kk & 3) * 32),
+                            mma_f16_ss(tmem + col_S(b), at(dK, sQ + qb * kSlotBytes + (kk >> 2) * kBoxBytes + (kk & 3) * 32),
                                        at(dK, kb + (kk >> 2) * kBoxBytes + (kk & 3) * 32), idS, kk > 0);
                         mma_commit(&sh.s_full[b]);
                         release(slot);
@@ -560,7 +570,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                     }
                 }
                 if (!ok) break;
-                if (is_s) mma_commit(&sh.q_empty);   // after the segment's last S MMA
+                if (is_s) mma_commit(&sh.q_empty[qb]);   // after the segment's last S MMA
                 else mma_commit(&sh.o_full);
                 ++nseg;
             }
@@ -589,6 +599,66 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         };
         auto grp_sync = [&]() { asm volatile("bar.sync 1, %0;" ::"n"(128 * SPL) : "memory"); };
         auto pair_sync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(2 + quad), "n"(32 * SPL) : "memory"); };
+        // Epilogue of a finished segment, run after the next segment's first tile (or after the last segment):
+        // the softmax works on that tile while the segment's last PV completes.  O is normalised (bf16, this
+        // warp's COLS d columns) into the output row or the partial slot, then released to the PV issuer.
+        struct Pending {
+            float m, l, sc, osc;
+            size_t out_row;
+            uint8_t* part;
+            uint32_t nseg;
+            bool valid, on;
+        } pend;
+        pend.on = false;
+        auto epilogue = [&]() {
+            if (wait(&sh.o_full, pend.nseg & 1)) tc_fence_after();
+            sh.lx[h][row] = pend.l;                   // the row's sum is split between the row's warps
+            pair_sync();
+            float l_tot = 0.f;
+#pragma unroll
+            for (int j = 0; j < SPL; ++j) l_tot += sh.lx[j][row];
+            if (!dead) {
+                const float m_log2 = pend.m * pend.sc;
+                const float inv_l = l_tot > 0.f ? pend.osc / l_tot : 0.f;
+                uint16_t* dst_row = (pend.part ? (uint16_t*)pend.part + (size_t)row * kD : (uint16_t*)a.out + pend.out_row * kD) + COLS * h;
+#pragma unroll
+                for (int c = 0; c < COLS / 32; ++c) {
+                    uint32_t o[32];
+                    __syncwarp();
+                    tmem_ld32(tmem + lane_addr + col_O() + COLS * h + 32 * c, o);
+                    tmem_ld_wait();
+                    if (pend.valid) {
+                        uint4* dst = (uint4*)(dst_row + c * 32);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            uint32_t v[4];
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(o[8 * e + 2 * q]) * inv_l,
+                                                                                __uint_as_float(o[8 * e + 2 * q + 1]) * inv_l);
+                                v[q] = *reinterpret_cast<const uint32_t*>(&b2);
+                            }
+                            dst[e] = make_uint4(v[0], v[1], v[2], v[3]);
+                        }
+                    }
+                }
+                if (pend.valid && h == 0) {
+                    if (pend.part) {
+                        float* ml = (float*)(pend.part + (size_t)kRows * kD * 2);
+                        ml[row] = m_log2;
+                        ml[kRows + row] = l_tot;
+                    } else if (a.lse) {
+                        a.lse[pend.out_row] = (m_log2 + __log2f(l_tot)) * 0.69314718055994531f;
+                    }
+                }
+                // O has been read: the PV issuer may start the next segment
+                tc_fence_before();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.o_free);
+            pend.on = false;
+        };
+
         SegIter si;
         si.init(a, plan, UQ, QG);
         Seg sg;
@@ -610,7 +680,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             // Q by TMA (the producer), or else first, so that S of the segment's first tile is computed while the
             // ancestors are walked: this warp's half (64 of 128 d) of the Q row -> shared memory, box h of the
             // K-major 128-byte-swizzled A operand of the S MMA (bf16, or rounded to f16 when the caches are
-            // e4m3).  The previous segment's S MMAs have completed: this warp waited for its O before reaching here.
+            // e4m3), once the previous segment's S MMAs have completed (its epilogue comes later).
+            const uint32_t qb = nseg % QB;
+            if (!q_tma && nseg >= (uint32_t)QB) wait(&sh.q_empty[qb], (nseg / QB - 1) & 1);
             if (!dead && !q_tma) {
                 const uint4* src = (const uint4*)((const uint16_t*)a.q + out_row * kD) + (COLS / 8) * h;
 #pragma unroll
@@ -623,12 +695,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                         v.w = pack2<true>(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
                     }
                     const int d8 = h * (COLS / 8) + c;   // 16-byte chunk of the row: box d8 / 8, chunk d8 % 8
-                    *(uint4*)(smem + kSmemQ + (d8 >> 3) * kBoxBytes + sw128_offset(row, d8 & 7)) = v;
+                    *(uint4*)(smem + kSmemQ + qb * kSlotBytes + (d8 >> 3) * kBoxBytes + sw128_offset(row, d8 & 7)) = v;
                 }
                 fence_proxy_async_smem();   // the MMAs (async proxy) read what this thread wrote
             }
             __syncwarp();
-            if (lane == 0 && !q_tma) mbar_arrive(&sh.q_full);
+            if (lane == 0 && !q_tma) mbar_arrive(&sh.q_full[qb]);
 
             // ancestors of this row's node from the request's parent array (walk bounded by T, so a malformed
             // array cannot trap; such requests are zeroed and flagged by the merge kernel)
@@ -797,56 +869,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&sh.p_full[bb]);
                 }
+                if (pend.on) epilogue();   // the previous segment's
             }
-            // epilogue: all MMAs of the segment are complete
-            if (wait(&sh.o_full, nseg & 1)) tc_fence_after();
-            ++nseg;
-            sh.lx[h][row] = l_run;                    // the row's sum is split between the row's warps
-            pair_sync();
-            float l_tot = 0.f;
-#pragma unroll
-            for (int j = 0; j < SPL; ++j) l_tot += sh.lx[j][row];
-            if (!dead) {
-                const float m_log2 = m_run * sc;
-                // normalised O (bf16, this warp's COLS d columns) either to the output row or to the partial slot
-                const float inv_l = l_tot > 0.f ? osc / l_tot : 0.f;
-                uint16_t* dst_row = (part ? (uint16_t*)part + (size_t)row * kD : (uint16_t*)a.out + out_row * kD) + COLS * h;
-#pragma unroll
-                for (int c = 0; c < COLS / 32; ++c) {
-                    uint32_t o[32];
-                    __syncwarp();
-                    tmem_ld32(tmem + lane_addr + col_O() + COLS * h + 32 * c, o);
-                    tmem_ld_wait();
-                    if (valid_row) {
-                        uint4* dst = (uint4*)(dst_row + c * 32);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            uint32_t v[4];
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(o[8 * e + 2 * q]) * inv_l,
-                                                                                __uint_as_float(o[8 * e + 2 * q + 1]) * inv_l);
-                                v[q] = *reinterpret_cast<const uint32_t*>(&b2);
-                            }
-                            dst[e] = make_uint4(v[0], v[1], v[2], v[3]);
-                        }
-                    }
-                }
-                if (valid_row && h == 0) {
-                    if (part) {
-                        float* ml = (float*)(part + (size_t)kRows * kD * 2);
-                        ml[row] = m_log2;
-                        ml[kRows + row] = l_tot;
-                    } else if (a.lse) {
-                        a.lse[out_row] = (m_log2 + __log2f(l_tot)) * 0.69314718055994531f;
-                    }
-                }
-                // O has been read: the PV issuer may start the next segment
-                tc_fence_before();
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.o_free);
+            // the segment's epilogue waits until the next segment's first tile is done (or the last segment ends)
+            pend.m = m_run;
+            pend.l = l_run;
+            pend.sc = sc;
+            pend.osc = osc;
+            pend.out_row = out_row;
+            pend.part = part;
+            pend.nseg = nseg++;
+            pend.valid = valid_row;
+            pend.on = true;
         }
+        if (pend.on) epilogue();
     }
     if (!active && tid == 0) {   // CTAs beyond the used grid complete no split unit
         SplitRec r = {};
