@@ -78,6 +78,8 @@ def load(path):
     L.or_accept.argtypes = [i, i, i, i, P, P, P, P, C.c_float, P, P, P, P, P, P, P]
     L.or_loss_f64.argtypes = [i, i, i, P] + [P] * 9
     L.or_loss.argtypes = [i, i, i, P] + [P] * 9
+    L.or_kv_compact.argtypes = [i, i, i, i, i, i, P, P, P, P, P, P, P, P]
+    L.or_tree_expand.argtypes = [i, i, i, i, i, i, P, P, P, P, P, P, P, P]
     return L
 
 
@@ -203,3 +205,36 @@ def loss_f64(logits, tokens, parent, labels, *, V, want_grad=True):
 
 def loss_w(lb, want_grad=True):
     return loss(lb.logits, lb.tokens, lb.parent, lb.labels, V=lb.V, want_grad=want_grad)
+
+
+# ------------------------------------------------------------------------------------------------ KV compaction
+def kv_compact(k, v, kv_len, parent, accept_len, path, *, kv_dt):
+    """Compaction of the accepted path's K/V.  Returns (k', v', new_kv_len, status, rc) on copies."""
+    k = np.array(k, copy=True, order="C")
+    v = np.array(v, copy=True, order="C")
+    B, Hkv, kv_cap, D = k.shape
+    T = parent.shape[1]
+    parent = np.ascontiguousarray(parent, np.int32)
+    kv_len = np.ascontiguousarray(kv_len, np.int32)
+    accept_len = np.ascontiguousarray(accept_len, np.int32)
+    path = np.ascontiguousarray(path, np.int32)
+    new_len = np.zeros(B, np.int32)
+    status = np.zeros(B, np.int32)
+    rc = lib().or_kv_compact(B, T, Hkv, D, kv_cap, DT[kv_dt], _p(k), _p(v), _p(kv_len), _p(parent),
+                             _p(accept_len), _p(path), _p(new_len), _p(status))
+    return k, v, new_len, status, rc
+
+
+# ------------------------------------------------------------------------------------------------ tree expansion
+def tree_expand(logits, front_score, *, V, k, n_keep, logit_dt):
+    """One level of draft tree expansion.  logits [B, n_front, V]; front_score [B, n_front] float32."""
+    logits = np.ascontiguousarray(logits)
+    fs = np.ascontiguousarray(front_score, np.float32)
+    B, n_front = fs.shape
+    res = dict(topk_token=np.zeros((B, n_front, k), np.int32), topk_logprob=np.zeros((B, n_front, k)),
+               child_parent=np.zeros((B, n_keep), np.int32), child_token=np.zeros((B, n_keep), np.int32),
+               child_score=np.zeros((B, n_keep)), status=np.zeros(B, np.int32))
+    res["rc"] = lib().or_tree_expand(B, n_front, V, k, n_keep, DT[logit_dt], _p(logits), _p(fs),
+                                     _p(res["topk_token"]), _p(res["topk_logprob"]), _p(res["child_parent"]),
+                                     _p(res["child_token"]), _p(res["child_score"]), _p(res["status"]))
+    return res

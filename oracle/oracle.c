@@ -475,3 +475,150 @@ int or_loss(int N, int T, int V, const uint16_t* logits_bf16, const int32_t* tok
     return loss_core(N, T, V, logits_bf16, 1, tokens, parent, labels, row_loss, row_acc, row_rej, sums,
                      grad, status);
 }
+
+/* ---------------------------------------------------------------------------------------------- */
+/* KV compaction after acceptance (plain definition)                                                */
+/* ---------------------------------------------------------------------------------------------- */
+/* After verification the request's committed tokens are the root plus the accepted path.  The root's K/V
+ * already sit at cache position L (the first tree slot) and the accepted node path[j] sits at L + path[j];
+ * compaction makes the committed tokens contiguous, so position L + 1 + j receives what was at
+ * L + path[j] ("Aurora" post, section 2: verification keeps the accepted continuation; TIDE overview:
+ * the target keeps the accepted draft tokens).  The new prefix length is L + 1 + accept_len; positions
+ * past it keep whatever they held.  This is the out-of-place definition: every read sees the cache as it
+ * was before the call.  A request whose accept_len is negative (a failed verification) or whose path is
+ * not a root path of its tree is left untouched (new length = old length) with a status code. */
+int or_kv_compact(int B, int T, int Hkv, int D, int kv_cap, int kv_dt, void* k_cache, void* v_cache,
+                  const int32_t* kv_len, const int32_t* parent, const int32_t* accept_len, const int32_t* path,
+                  int32_t* new_kv_len, int32_t* status) {
+    if (B < 0 || T < 1 || Hkv < 1 || D < 1 || kv_cap < T) return E_ARG;
+    if (T > 64) return E_BIG;
+    if (kv_dt != DT_F32 && kv_dt != DT_BF16 && kv_dt != DT_E4M3) return E_UNSUP;
+    size_t esz = kv_dt == DT_F32 ? 4 : kv_dt == DT_BF16 ? 2 : 1;
+    size_t row = (size_t)D * esz;
+    unsigned char* old = (unsigned char*)malloc(row * (size_t)T);
+    for (int b = 0; b < B; ++b) {
+        const int32_t* par = parent + (size_t)b * T;
+        const int32_t* pth = path + (size_t)b * T;
+        int L = kv_len[b], n = accept_len[b];
+        int st = or_tree_check(T, par);
+        if (!st && (L < 0 || (long)L + T > kv_cap)) st = E_ARG;
+        if (!st && (n < 0 || n > T - 1)) st = E_ARG;
+        /* the path must walk down the tree from the root: path[0] a child of 0, path[j] a child of path[j-1] */
+        for (int j = 0; !st && j < n; ++j) {
+            int node = pth[j], up = j == 0 ? 0 : pth[j - 1];
+            if (node < 1 || node >= T || par[node] != up) st = E_ARG;
+        }
+        status[b] = st;
+        new_kv_len[b] = st ? L : L + 1 + n;
+        if (st) continue;
+        for (int h = 0; h < Hkv; ++h) {
+            for (int c = 0; c < 2; ++c) {
+                unsigned char* cache = (unsigned char*)(c == 0 ? k_cache : v_cache);
+                unsigned char* base = cache + (((size_t)b * Hkv + h) * (size_t)kv_cap + (size_t)L) * row;
+                memcpy(old, base, row * (size_t)T);             /* the tree block as it was */
+                for (int j = 0; j < n; ++j) memcpy(base + (size_t)(1 + j) * row, old + (size_t)pth[j] * row, row);
+            }
+        }
+    }
+    free(old);
+    return OK;
+}
+
+/* ---------------------------------------------------------------------------------------------- */
+/* Draft tree expansion, one level (plain definition, float64)                                      */
+/* ---------------------------------------------------------------------------------------------- */
+/* The draft proposes the next level of its tree from the logits of the current frontier ("Aurora" post,
+ * section 2, and the TIDE overview: the draft proposes tokens that the target then verifies in one pass).
+ * Row s of a request is the draft's next-token logits after frontier node s, whose path score (the sum of
+ * the draft's log-probabilities along the path from the root) is front_score[s].  Each row proposes its
+ * k most likely tokens (largest logit first, lower token id first on equal logits), with log-probability
+ * z - logsumexp(row) at temperature 1.  A candidate's score is its parent's score plus its log-probability;
+ * the n_keep best candidates of the request survive (higher score first, then lower frontier slot, then
+ * lower rank), and they are listed in (frontier slot, rank) order, the breadth-first numbering of the next
+ * level.  Outputs per request: topk_token / topk_logprob [n_front, k], child_parent (frontier slot) /
+ * child_token / child_score [n_keep].  A request with a non-finite logit or score gets status 5 and -1 /
+ * -inf outputs. */
+typedef struct { double score; int slot, rank; } or_cand;
+
+static int cand_cmp(const void* a, const void* b) {
+    const or_cand* x = (const or_cand*)a;
+    const or_cand* y = (const or_cand*)b;
+    if (x->score != y->score) return x->score > y->score ? -1 : 1;
+    if (x->slot != y->slot) return x->slot < y->slot ? -1 : 1;
+    return x->rank < y->rank ? -1 : (x->rank > y->rank);
+}
+
+static int cand_bfs_cmp(const void* a, const void* b) {
+    const or_cand* x = (const or_cand*)a;
+    const or_cand* y = (const or_cand*)b;
+    if (x->slot != y->slot) return x->slot < y->slot ? -1 : 1;
+    return x->rank < y->rank ? -1 : (x->rank > y->rank);
+}
+
+int or_tree_expand(int B, int n_front, int V, int k, int n_keep, int logit_dt, const void* logits,
+                   const float* front_score, int32_t* topk_token, double* topk_logprob, int32_t* child_parent,
+                   int32_t* child_token, double* child_score, int32_t* status) {
+    if (B < 0 || n_front < 1 || V < 1 || k < 1 || k > V || n_keep < 0 || n_keep > n_front * k) return E_ARG;
+    if (logit_dt != DT_F32 && logit_dt != DT_BF16) return E_UNSUP;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        int st = OK;
+        or_cand* cand = (or_cand*)malloc(sizeof(or_cand) * (size_t)n_front * k);
+        char* taken = (char*)malloc((size_t)V);
+        for (int s = 0; s < n_front && !st; ++s) {
+            size_t r = (size_t)b * n_front + s;
+            if (!isfinite(front_score[r])) { st = E_NONFINITE; break; }
+            double m = -INFINITY;
+            for (int j = 0; j < V; ++j) {
+                float z = load_logit(logits, r * V + j, logit_dt);
+                if (!isfinite(z)) { st = E_NONFINITE; break; }
+                if (z > m) m = z;
+            }
+            if (st) break;
+            double sum = 0.0;
+            for (int j = 0; j < V; ++j) sum += exp((double)load_logit(logits, r * V + j, logit_dt) - m);
+            double lse = m + log(sum);
+            /* k rounds of "largest remaining logit, lowest id on ties" */
+            memset(taken, 0, (size_t)V);
+            for (int q = 0; q < k; ++q) {
+                int best = -1;
+                float bz = 0.f;
+                for (int j = 0; j < V; ++j) {
+                    if (taken[j]) continue;
+                    float z = load_logit(logits, r * V + j, logit_dt);
+                    if (best < 0 || z > bz) { best = j; bz = z; }
+                }
+                taken[best] = 1;
+                topk_token[r * k + q] = best;
+                topk_logprob[r * k + q] = (double)bz - lse;
+                cand[s * k + q].score = (double)front_score[r] + ((double)bz - lse);
+                cand[s * k + q].slot = s;
+                cand[s * k + q].rank = q;
+            }
+        }
+        if (st) {
+            for (int i = 0; i < n_front * k; ++i) {
+                topk_token[(size_t)b * n_front * k + i] = -1;
+                topk_logprob[(size_t)b * n_front * k + i] = -INFINITY;
+            }
+            for (int i = 0; i < n_keep; ++i) {
+                child_parent[(size_t)b * n_keep + i] = -1;
+                child_token[(size_t)b * n_keep + i] = -1;
+                child_score[(size_t)b * n_keep + i] = -INFINITY;
+            }
+        } else {
+            qsort(cand, (size_t)n_front * k, sizeof(or_cand), cand_cmp);   /* best first */
+            qsort(cand, (size_t)n_keep, sizeof(or_cand), cand_bfs_cmp);    /* survivors in BFS order */
+            for (int i = 0; i < n_keep; ++i) {
+                size_t r = (size_t)b * n_front + cand[i].slot;
+                child_parent[(size_t)b * n_keep + i] = cand[i].slot;
+                child_token[(size_t)b * n_keep + i] = topk_token[r * k + cand[i].rank];
+                child_score[(size_t)b * n_keep + i] = cand[i].score;
+            }
+        }
+        status[b] = st;
+        free(cand);
+        free(taken);
+    }
+    return OK;
+}

@@ -55,6 +55,20 @@ int or_loss(int N, int T, int V, const uint16_t* logits_bf16, const int32_t* tok
             const int32_t* labels, double* row_loss, double* row_acc, double* row_rej, double* sums,
             double* grad, int32_t* status);
 
+/* KV compaction after acceptance: position kv_len[b] + 1 + j of every kv head receives what was at
+ * kv_len[b] + path[b, j] (j < accept_len[b]); new_kv_len[b] = kv_len[b] + 1 + accept_len[b].  In place on
+ * k_cache / v_cache ([B, Hkv, kv_cap, D] in kv_dt), read-before-write semantics.  status[b]: 0, 1 (bad
+ * length or path), 2 (bad tree).  Returns 0 or an argument error. */
+int or_kv_compact(int B, int T, int Hkv, int D, int kv_cap, int kv_dt, void* k_cache, void* v_cache,
+                  const int32_t* kv_len, const int32_t* parent, const int32_t* accept_len, const int32_t* path,
+                  int32_t* new_kv_len, int32_t* status);
+
+/* One level of draft tree expansion: per frontier row the top-k tokens with log-probabilities (float64),
+ * then the n_keep best candidates of each request by path score, listed in (slot, rank) order. */
+int or_tree_expand(int B, int n_front, int V, int k, int n_keep, int logit_dt, const void* logits,
+                   const float* front_score, int32_t* topk_token, double* topk_logprob, int32_t* child_parent,
+                   int32_t* child_token, double* child_score, int32_t* status);
+
 /* Number of OpenMP threads the oracle will use (1 when built without OpenMP). */
 int or_num_threads(void);
 

@@ -327,6 +327,76 @@ def make_loss(seed: int, *, N: int, T: int, V: int, tree=(4, 3, 2, 1, 1), sigma:
 
 
 # ----------------------------------------------------------------------------------------------------
+# KV compaction inputs: accepted root paths
+# ----------------------------------------------------------------------------------------------------
+def random_root_paths(seed: int, parent: np.ndarray, stop_p: float = 0.3, full_p: float = 0.2):
+    """For every request a root path drawn by a random walk: from the current node, stop with probability
+    stop_p, else step to a uniformly chosen child; with probability full_p the walk never stops early
+    (it runs to a leaf).  Returns accept_len [B] int32 and path [B,T] int32 (-1 padded)."""
+    s_walk, s_full = rng_streams(seed, 2)
+    B, T = parent.shape
+    accept_len = np.zeros(B, np.int32)
+    path = np.full((B, T), -1, np.int32)
+    for b in range(B):
+        ch = children_of(parent[b])
+        full = s_full.random() < full_p
+        cur, n = 0, 0
+        while ch[cur] and (full or s_walk.random() >= stop_p):
+            cur = ch[cur][int(s_walk.integers(0, len(ch[cur])))]
+            path[b, n] = cur
+            n += 1
+        accept_len[b] = n
+    return accept_len, path
+
+
+# ----------------------------------------------------------------------------------------------------
+# draft tree expansion inputs: one level's frontier logits and path scores
+# ----------------------------------------------------------------------------------------------------
+@dataclass
+class Expand:
+    B: int
+    n_front: int
+    V: int
+    k: int
+    n_keep: int
+    logit_dt: str
+    logits: np.ndarray        # [B, n_front, V] draft logits of the frontier nodes
+    front_score: np.ndarray   # [B, n_front] float32 path scores (sums of log-probabilities, <= 0)
+    name: str = ""
+    meta: dict = field(default_factory=dict)
+
+
+def make_expand(seed: int, *, B: int, n_front: int, V: int, k: int, n_keep: int, logit_dt: str = "bf16",
+                sigma: float = 3.0, score_range: float = 6.0, ties: int = 0, name: str = "") -> Expand:
+    """Frontier logits ~ N(0, sigma^2) and path scores uniform in [-score_range, 0] (the root's is 0 when
+    n_front == 1).  ties > 0 plants, in every row, `ties` extra copies of the row maximum at random
+    positions so that the lower-token-first rule decides the order."""
+    s_z, s_score, s_tie = rng_streams(seed, 3)
+    zf = sigma * s_z.standard_normal(size=(B, n_front, V), dtype=np.float32)
+    if ties:
+        enc = decode_f32(encode(zf, logit_dt), logit_dt)
+        for b in range(B):
+            for s in range(n_front):
+                pos = s_tie.choice(V, size=min(ties, V), replace=False)
+                zf[b, s, pos] = enc[b, s].max()
+        del enc
+    logits = encode(zf, logit_dt)
+    if n_front == 1:
+        front = np.zeros((B, 1), np.float32)
+    else:
+        front = (-score_range * s_score.random(size=(B, n_front))).astype(np.float32)
+    return Expand(B=B, n_front=n_front, V=V, k=k, n_keep=n_keep, logit_dt=logit_dt, logits=logits,
+                  front_score=front, name=name, meta=dict(seed=seed, sigma=sigma))
+
+
+def expansion_levels(T: int, branching) -> list[tuple[int, int, int]]:
+    """(n_front, k, n_keep) of every level of a budgeted tree with the given node count and branching:
+    the level sizes of the tree generator above, expanded level by level."""
+    sizes = level_sizes(T, branching)
+    return [(sizes[d - 1], branching[d - 1], sizes[d]) for d in range(1, len(sizes))]
+
+
+# ----------------------------------------------------------------------------------------------------
 # named workloads (the shapes of the pages' serving setups; see DESIGN.md for the recipe)
 # ----------------------------------------------------------------------------------------------------
 WORKLOADS = {

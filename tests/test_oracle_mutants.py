@@ -12,6 +12,8 @@ import pytest
 import oracle
 from tests import test_oracle_accept as TA
 from tests import test_oracle_attn as TT
+from tests import test_oracle_compact as TC
+from tests import test_oracle_expand as TE
 from tests import test_oracle_loss as TL
 
 MUTANTS = {
@@ -38,6 +40,16 @@ MUTANTS = {
     "rejection_term_uses_log_q": (
         "rej += -log1mexp(a);", "rej += a;",
         TL.test_binary_vocab_rejection_is_cross_entropy_on_the_other_token),
+    "compact_destination_off_by_one": (
+        "memcpy(base + (size_t)(1 + j) * row,", "memcpy(base + (size_t)j * row,",
+        lambda: TC.test_path_nodes_see_a_causal_prefix_after_compaction("bf16", (3, 2, 2), 13)),
+    "expand_ties_take_last_token": (
+        "if (best < 0 || z > bz) { best = j; bz = z; }", "if (best < 0 || z >= bz) { best = j; bz = z; }",
+        lambda: TE.test_row_proposals_match_stable_sort_and_log_softmax("bf16", 3000, 3, 2)),
+    "expand_score_drops_parent_path": (
+        "cand[s * k + q].score = (double)front_score[r] + ((double)bz - lse);",
+        "cand[s * k + q].score = ((double)bz - lse);",
+        lambda: TE.test_selection_equals_brute_force_over_all_children(12, 5, 5)),
     "fx_poly_drops_cubic": (
         "p = fmaf(p, f, C_P3);", "p = fmaf(p, f, 0.0f);", TA.test_fx_exp2_polynomial_error_bound),
 }
