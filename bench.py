@@ -41,6 +41,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
+    ap.add_argument("--ops", nargs="*", default=None,
+                    help="instead of the step: time every library call on the named workloads (all if none given), "
+                         "one JSON line per call")
     return ap.parse_args()
 
 
@@ -159,6 +162,172 @@ def traffic_from_profile(kernel_src: Path, workload: str):
         return None
     h = hashlib.sha256(kernel_src.read_bytes()).hexdigest()[:16]
     return d["traffic_bytes_per_launch"] if d.get("source_sha") == h else None
+
+
+# ------------------------------------------------------------------------------------------ per-call timings
+def run_ops(args):
+    """One JSON line per (workload, call): median of 10 CUDA-graph replays, each after a 256 MB L2 flush,
+    with the call's algorithmic bytes and the fraction of the HBM peak they represent."""
+    import torch
+
+    from speculative_decoding_tree_verify_gb300 import sv
+    from speculative_decoding_tree_verify_gb300 import workloads as W
+
+    peak, peak_kind = peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(args.seed)
+
+    def dev(a):
+        if a is None:
+            return None
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        elif a.dtype == np.uint32:
+            a = a.view(np.int32)
+        return torch.from_numpy(a).cuda()
+
+    def timed(fn, reps=10):
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            fn()
+            fn()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3)
+        return float(np.median(ts))
+
+    def report(name, op, us, nbytes, note=""):
+        gbs = nbytes / (us * 1e-6) / 1e9
+        print(json.dumps({"workload": name, "op": op, "us": round(us, 1), "alg_MB": round(nbytes / 1e6, 3),
+                          "GB_s": round(gbs, 1), "frac": round(gbs / peak, 3), "peak_kind": peak_kind,
+                          "note": note}), flush=True)
+
+    i32 = dict(dtype=torch.int32, device="cuda")
+
+    def attn_case(name, w, device_kv=False):
+        q = dev(w.q)
+        if device_kv:   # timing only: seeded random cache codes of the right dtype, drawn on the device
+            shape = (w.B, w.Hkv, w.kv_cap, w.D)
+            if w.kv_dt == "e4m3":
+                k = torch.randint(0, 0x7E, shape, dtype=torch.uint8, device="cuda", generator=gen)
+                v = torch.randint(0, 0x7E, shape, dtype=torch.uint8, device="cuda", generator=gen)
+            else:
+                k = torch.randn(shape, device="cuda", generator=gen).to(torch.bfloat16).view(torch.int16)
+                v = torch.randn(shape, device="cuda", generator=gen).to(torch.bfloat16).view(torch.int16)
+            ks = torch.full((w.Hkv,), 0.01, device="cuda")
+            vs = ks.clone()
+        else:
+            k, v, ks, vs = dev(w.k), dev(w.v), dev(w.k_scale), dev(w.v_scale)
+        if q is None:
+            q = torch.randn((w.B, w.T, w.Hq, w.D), device="cuda", generator=gen).to(torch.bfloat16).view(torch.int16)
+        out = torch.empty_like(q)
+        lse = torch.empty((w.B, w.T, w.Hq), dtype=torch.float32, device="cuda")
+        st = torch.empty((w.B,), **i32)
+        n = sv.workspace_size(sv.OP_TREE_ATTN, w.B, w.T, w.Hq, w.Hkv, w.D, w.kv_cap, 0)
+        ws = torch.empty(max(n, 256), dtype=torch.uint8, device="cuda")
+        kl, par = dev(w.kv_len), dev(w.parent)
+        fn = lambda: sv.tree_attn(q, k, v, kl, par, out, k_scale=ks, v_scale=vs, lse=lse, status=st, workspace=ws)
+        us = timed(fn, reps=5 if w.kv_dt == "e4m3" else 10)
+        tc = w.q_dt == "bf16" and w.kv_dt in ("bf16", "e4m3") and w.D == 128
+        report(name, "tree_attn", us, attn_bytes(w), "tensor cores" if tc else "CUDA cores")
+
+    def accept_case(name, w, temperature, draft):
+        B, T, V = w.B, w.T, w.V
+        tgt = dev(w.target_logits).view(B, T, V)
+        dr = dev(draft).view(B, T, V) if draft is not None else None
+        tok, par, u = dev(w.tokens), dev(w.parent), dev(w.uniforms)
+        outs = [torch.empty((B,), **i32), torch.empty((B, T), **i32), torch.empty((B, T), **i32),
+                torch.empty((B,), **i32)]
+        st = torch.empty((B,), **i32)
+        ws = torch.empty(max(sv.workspace_size(sv.OP_ACCEPT, B, T, V=V), 256), dtype=torch.uint8, device="cuda")
+        fn = lambda: sv.accept(tgt, tok, par, *outs, draft_logits=dr, temperature=temperature, uniforms=u, status=st,
+                               workspace=ws)
+        us = timed(fn)
+        rows = B * T * (2 if dr is not None else 1)
+        mode = "greedy" if temperature == 0 else ("prob" if dr is not None else "onehot")
+        report(name, f"accept_{mode}", us, rows * V * ES[w.logit_dt] + B * T * 24)
+
+    def loss_case(name, lb):
+        N, T, V = lb.N, lb.T, lb.V
+        z, tok, par, lab = dev(lb.logits), dev(lb.tokens), dev(lb.parent), dev(lb.labels)
+        rl = torch.empty((N * T,), dtype=torch.float32, device="cuda")
+        sums = torch.empty((3,), dtype=torch.float32, device="cuda")
+        grad = torch.empty_like(z)
+        st = torch.empty((N,), **i32)
+        ws = torch.empty(max(sv.workspace_size(sv.OP_LOSS, N, T, V=V), 256), dtype=torch.uint8, device="cuda")
+        fn = lambda: sv.loss(z, tok, par, lab, rl, sums, grad=grad, status=st, workspace=ws)
+        report(name, "loss+grad", timed(fn), 2 * N * T * V * 2 + N * T * 16)
+
+    def compact_case(name, B, T, Hkv, D, kv_cap, kv_dt, kv_len, parent, seed):
+        """KV compaction of random accepted root paths; bytes = the moved rows read once and written once."""
+        shape = (B, Hkv, kv_cap, D)
+        dt = {"e4m3": torch.uint8, "bf16": torch.int16, "f32": torch.float32}[kv_dt]
+        k = torch.zeros(shape, dtype=dt, device="cuda")
+        v = torch.zeros_like(k)
+        acc, path = W.random_root_paths(seed, parent)
+        kl, par, al, pth = dev(kv_len), dev(parent), dev(acc), dev(path)
+        nl = torch.empty((B,), **i32)
+        st = torch.empty((B,), **i32)
+        fn = lambda: sv.kv_compact(k, v, kl, par, al, pth, nl, status=st)
+        moved = sum(int(np.sum(path[b, :acc[b]] != np.arange(1, acc[b] + 1))) for b in range(B))
+        report(name, "kv_compact", timed(fn), moved * Hkv * D * ES[kv_dt] * 2 * 2,
+               f"mean accept_len {float(np.mean(acc)):.2f}, launch-bound")
+
+    def expand_case(name, B, V, levels, sigma, seed):
+        """Every level of the tree, one call each; bytes = the frontier logit rows read once."""
+        tot_us, tot_b = 0.0, 0
+        for d, (nf, kk, nk) in enumerate(levels):
+            e = W.make_expand(seed + d, B=B, n_front=nf, V=V, k=kk, n_keep=nk, logit_dt="bf16", sigma=sigma)
+            z, fs = dev(e.logits).view(B, nf, V), dev(e.front_score)
+            tt = torch.empty((B, nf, kk), **i32)
+            tl = torch.empty((B, nf, kk), dtype=torch.float32, device="cuda")
+            cp, ct = torch.empty((B, max(nk, 1)), **i32), torch.empty((B, max(nk, 1)), **i32)
+            cs = torch.empty((B, max(nk, 1)), dtype=torch.float32, device="cuda")
+            st = torch.empty((B,), **i32)
+            fn = lambda: sv.tree_expand(z, fs, kk, nk, tt, tl, cp, ct, cs, status=st)
+            us = timed(fn)
+            nb = B * nf * V * 2
+            tot_us += us
+            tot_b += nb
+            report(name, f"tree_expand_level{d + 1}", us, nb, f"{nf} x top-{kk} -> {nk}")
+        report(name, "tree_expand_all_levels", tot_us, tot_b, f"{len(levels)} calls")
+
+    which = args.ops or ["tiny_chain", "llama3_8b_tree", "qwen3_8b_stochastic", "loss_batch", "fp8_long_context"]
+    for name in which:
+        if name == "loss_batch":
+            loss_case(name, W.make_workload(name, seed=args.seed))
+            continue
+        if name == "fp8_long_context":
+            w = W.make_workload(name, seed=args.seed, with_attn=False)
+            accept_case(name, w, 0.0, None)
+            w2 = W.make_workload(name, seed=args.seed, with_attn=False, mode="onehot", temperature=0.7)
+            accept_case(name, w2, 0.7, None)
+            del w2
+            attn_case(name, w, device_kv=True)
+            compact_case(name, w.B, w.T, w.Hkv, w.D, w.kv_cap, w.kv_dt, w.kv_len, w.parent, args.seed)
+            expand_case(name, w.B, w.V, W.expansion_levels(64, (4, 3, 2, 2, 1, 1, 1)), 3.0, 500 + args.seed)
+            continue
+        w = W.make_workload(name, seed=args.seed)
+        attn_case(name, w)
+        accept_case(name, w, w.temperature, w.draft_logits if w.temperature > 0 else None)
+        compact_case(name, w.B, w.T, w.Hkv, w.D, w.kv_cap, w.kv_dt, w.kv_len, w.parent, args.seed)
+        if name == "llama3_8b_tree":
+            expand_case(name, w.B, w.V, W.expansion_levels(60, (4, 3, 2, 2, 1, 1)), 3.0, 200 + args.seed)
+        elif name == "qwen3_8b_stochastic":
+            expand_case(name, w.B, w.V, [(1, 1, 1)] * 5, 2.5, 300 + args.seed)
 
 
 # ------------------------------------------------------------------------------------------ main arms
@@ -346,6 +515,10 @@ def main():
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.ops is not None:
+        if rank == 0:
+            run_ops(args)
         return
     if world > 1:
         import torch

@@ -180,6 +180,61 @@ sv_status sv_loss(int N, int T, int V, const void* draft_logits, const int32_t* 
                   const int32_t* parent, const int32_t* labels, float* row_loss, float* sums, void* grad,
                   int32_t* status, void* workspace, size_t ws_bytes, sv_stream_t stream);
 
+/*
+ * sv_kv_compact -- make the accepted path's K/V contiguous after verification.
+ *
+ * After sv_accept the committed tokens of request b are the root plus the accepted path ("Aurora" post,
+ * section 2, and the TIDE overview: the target keeps the accepted continuation of the draft).  The root's
+ * K/V are at cache position L = kv_len[b] (the first tree slot) and accepted node path[b, j] at
+ * L + path[b, j]; this call moves them so that, for every kv head,
+ *     K/V[b, :, L + 1 + j, :]  <-  K/V[b, :, L + path[b, j], :]      j = 0 .. accept_len[b] - 1
+ * with every read seeing the cache as it was before the call, and writes new_kv_len[b] = L + 1 +
+ * accept_len[b]: the next verification step sees a causal prefix.  Positions past the new length keep
+ * whatever they held.  The copy is in place on the caches; it moves bytes, so the result is exact for
+ * every kv_dt.
+ *   k_cache, v_cache  [B, Hkv, kv_cap, D] in kv_dt (SV_F32, SV_BF16 or SV_E4M3 codes); D * element size
+ *                     must be a multiple of 16 bytes and at most 8192
+ *   kv_len     int32 [B]     the prefix length the tree was verified against
+ *   parent     int32 [B, T]  the verified tree
+ *   accept_len int32 [B], path int32 [B, T]: as written by sv_accept
+ *   new_kv_len int32 [B]     output; must not alias kv_len
+ *   status     int32 [B] or NULL: SV_ERR_BAD_TREE for a malformed parent array, SV_ERR_INVALID_ARG for
+ *              accept_len < 0 (a failed verification) or > T - 1, a path that is not a walk down the tree
+ *              from the root, or kv_len + T > kv_cap.  Such a request is left untouched and its
+ *              new_kv_len is kv_len.
+ * No workspace.  Requests and kv heads are independent CTAs; the call never reads positions below L.
+ */
+sv_status sv_kv_compact(int B, int T, int Hkv, int D, int kv_cap, sv_dtype kv_dt, void* k_cache, void* v_cache,
+                        const int32_t* kv_len, const int32_t* parent, const int32_t* accept_len,
+                        const int32_t* path, int32_t* new_kv_len, int32_t* status, sv_stream_t stream);
+
+/*
+ * sv_tree_expand -- one level of draft tree expansion, the step that builds the tree verified next.
+ *
+ * The draft proposes the tokens the target then verifies in one pass ("Aurora" post, section 2; TIDE
+ * overview).  Row s of request b (logits[b, s, :]) is the draft's next-token logits after frontier node s,
+ * whose path score front_score[b, s] is the sum of the draft's log-probabilities from the root (0 for the
+ * root).  Each row proposes its k most likely tokens: larger logit first, lower token id first on equal
+ * logits, with log-probability z - logsumexp(row) at temperature 1.  A candidate's score is its frontier
+ * node's score plus its log-probability; the n_keep best candidates of the request survive (higher score
+ * first, then lower slot, then lower rank) and are listed in (slot, rank) order, which is the breadth-first
+ * numbering of the next level.  Calling this once per level with (n_front, k, n_keep) = (n_{d-1}, k_d, n_d)
+ * builds a tree with a fixed node budget per level.
+ *   logits       [B, n_front, V] in logit_dt (SV_F32 or SV_BF16)
+ *   front_score  float [B, n_front]
+ *   topk_token   int32 [B, n_front, k], topk_logprob float [B, n_front, k]   (outputs, required)
+ *   child_parent int32 [B, n_keep] frontier slot of each survivor; child_token int32 [B, n_keep];
+ *   child_score  float [B, n_keep] = front_score + log-probability, rounded to float32 once
+ *   status       int32 [B] or NULL: SV_ERR_NONFINITE when a row of the request holds NaN/Inf or its
+ *                front_score is not finite; that request's outputs are -1 (tokens, slots) and -inf.
+ * Limits: 1 <= k <= min(16, V), n_front * k <= 1024, 0 <= n_keep <= n_front * k.  Log-probabilities are
+ * computed in float32 (the scores of two candidates closer than about 1e-5 may rank differently from an
+ * exact computation).  No workspace.
+ */
+sv_status sv_tree_expand(int B, int n_front, int V, int k, int n_keep, sv_dtype logit_dt, const void* logits,
+                         const float* front_score, int32_t* topk_token, float* topk_logprob, int32_t* child_parent,
+                         int32_t* child_token, float* child_score, int32_t* status, sv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

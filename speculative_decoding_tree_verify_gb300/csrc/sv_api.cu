@@ -142,4 +142,41 @@ sv_status sv_loss(int N, int T, int V, const void* draft_logits, const int32_t* 
     return from_cuda(launch_loss(a, (cudaStream_t)stream));
 }
 
+sv_status sv_kv_compact(int B, int T, int Hkv, int D, int kv_cap, sv_dtype kv_dt, void* k_cache, void* v_cache,
+                        const int32_t* kv_len, const int32_t* parent, const int32_t* accept_len,
+                        const int32_t* path, int32_t* new_kv_len, int32_t* status, sv_stream_t stream) {
+    if (T > SV_MAX_T) return SV_ERR_TREE_TOO_LARGE;
+    if (B < 0 || B > 65535 || T < 1 || Hkv < 1 || D < 1 || kv_cap < T || (long long)B * Hkv > 0x7fffffffLL)
+        return SV_ERR_INVALID_ARG;
+    if (kv_dt != SV_F32 && kv_dt != SV_BF16 && kv_dt != SV_E4M3) return SV_ERR_UNSUPPORTED;
+    const int esz = kv_dt == SV_F32 ? 4 : kv_dt == SV_BF16 ? 2 : 1;
+    if ((D * esz) % 16 || D * esz > 8192) return SV_ERR_UNSUPPORTED;
+    if (B == 0) return SV_OK;
+    if (!k_cache || !v_cache || !kv_len || !parent || !accept_len || !path || !new_kv_len) return SV_ERR_INVALID_ARG;
+    if ((const void*)new_kv_len == (const void*)kv_len) return SV_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(kv_len, 4) || !aligned(parent, 4) ||
+        !aligned(accept_len, 4) || !aligned(path, 4) || !aligned(new_kv_len, 4) || !aligned(status, 4))
+        return SV_ERR_UNSUPPORTED;
+    CompactArgs a{B, T, Hkv, D, kv_cap, kv_dt, k_cache, v_cache, kv_len, parent, accept_len, path, new_kv_len, status};
+    return from_cuda(launch_kv_compact(a, (cudaStream_t)stream));
+}
+
+sv_status sv_tree_expand(int B, int n_front, int V, int k, int n_keep, sv_dtype logit_dt, const void* logits,
+                         const float* front_score, int32_t* topk_token, float* topk_logprob, int32_t* child_parent,
+                         int32_t* child_token, float* child_score, int32_t* status, sv_stream_t stream) {
+    if (B < 0 || B > 65535 || n_front < 1 || V < 1 || k < 1 || k > V || n_keep < 0) return SV_ERR_INVALID_ARG;
+    if (k > SV_MAX_EXPAND_K || n_front * k > SV_MAX_EXPAND_CAND || n_keep > n_front * k) return SV_ERR_INVALID_ARG;
+    if ((long long)B * n_front * 8 > 0x7fffffffLL) return SV_ERR_INVALID_ARG;
+    if (logit_dt != SV_F32 && logit_dt != SV_BF16) return SV_ERR_UNSUPPORTED;
+    if (B == 0) return SV_OK;
+    if (!logits || !front_score || !topk_token || !topk_logprob) return SV_ERR_INVALID_ARG;
+    if (n_keep > 0 && (!child_parent || !child_token || !child_score)) return SV_ERR_INVALID_ARG;
+    if (!aligned(logits, 16) || !aligned(front_score, 4) || !aligned(topk_token, 4) || !aligned(topk_logprob, 4) ||
+        !aligned(child_parent, 4) || !aligned(child_token, 4) || !aligned(child_score, 4) || !aligned(status, 4))
+        return SV_ERR_UNSUPPORTED;
+    ExpandArgs a{B, n_front, V, k, n_keep, logit_dt, logits, front_score, topk_token, topk_logprob, child_parent,
+                 child_token, child_score, status};
+    return from_cuda(launch_tree_expand(a, (cudaStream_t)stream));
+}
+
 }  // extern "C"

@@ -122,6 +122,39 @@ struct LossArgs {
 size_t loss_workspace_size(int N, int T, int V);
 cudaError_t launch_loss(const LossArgs& a, cudaStream_t s);
 
+struct CompactArgs {
+    int B, T, Hkv, D, kv_cap;
+    sv_dtype kv_dt;
+    void* k;
+    void* v;
+    const int32_t* kv_len;
+    const int32_t* parent;
+    const int32_t* accept_len;
+    const int32_t* path;
+    int32_t* new_kv_len;
+    int32_t* status;
+};
+
+cudaError_t launch_kv_compact(const CompactArgs& a, cudaStream_t s);
+
+struct ExpandArgs {
+    int B, n_front, V, k, n_keep;
+    sv_dtype logit_dt;
+    const void* logits;
+    const float* front_score;
+    int32_t* topk_token;
+    float* topk_logprob;
+    int32_t* child_parent;
+    int32_t* child_token;
+    float* child_score;
+    int32_t* status;
+};
+
+#define SV_MAX_EXPAND_K 16
+#define SV_MAX_EXPAND_CAND 1024
+
+cudaError_t launch_tree_expand(const ExpandArgs& a, cudaStream_t s);
+
 // Launch with an optional thread-block cluster and programmatic dependent launch.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,

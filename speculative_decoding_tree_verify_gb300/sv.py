@@ -49,6 +49,10 @@ def lib() -> C.CDLL:
         L.sv_loss.restype = i
         L.sv_accept_noalloc.argtypes = [i, i, i, i, P, P, P, P, f, P, P, P, P, P, P, P, P]
         L.sv_accept_noalloc.restype = i
+        L.sv_kv_compact.argtypes = [i, i, i, i, i, i, P, P, P, P, P, P, P, P, P]
+        L.sv_kv_compact.restype = i
+        L.sv_tree_expand.argtypes = [i, i, i, i, i, i, P, P, P, P, P, P, P, P, P]
+        L.sv_tree_expand.restype = i
         _lib = L
     return _lib
 
@@ -145,3 +149,23 @@ def loss(draft_logits, tokens, parent, labels, row_loss, sums, *, grad=None, sta
                          _ptr(sums), _ptr(grad), _ptr(status), _ptr(ws), ws.numel() * ws.element_size(),
                          _stream(stream))
     _check(code, "sv_loss")
+
+
+def kv_compact(k_cache, v_cache, kv_len, parent, accept_len, path, new_kv_len, *, status=None, stream=None):
+    """sv_kv_compact: caches [B,Hkv,kv_cap,D] (modified in place); kv_len/accept_len/new_kv_len [B]; parent/path [B,T]."""
+    B, Hkv, kv_cap, D = k_cache.shape
+    T = parent.shape[1]
+    code = lib().sv_kv_compact(B, T, Hkv, D, kv_cap, dtype_code(k_cache), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len),
+                               _ptr(parent), _ptr(accept_len), _ptr(path), _ptr(new_kv_len), _ptr(status),
+                               _stream(stream))
+    _check(code, "sv_kv_compact")
+
+
+def tree_expand(logits, front_score, k, n_keep, topk_token, topk_logprob, child_parent, child_token, child_score, *,
+                status=None, stream=None):
+    """sv_tree_expand: logits [B,n_front,V]; front_score [B,n_front]; topk_* [B,n_front,k]; child_* [B,n_keep]."""
+    B, n_front, V = logits.shape
+    code = lib().sv_tree_expand(B, n_front, V, int(k), int(n_keep), dtype_code(logits), _ptr(logits),
+                                _ptr(front_score), _ptr(topk_token), _ptr(topk_logprob), _ptr(child_parent),
+                                _ptr(child_token), _ptr(child_score), _ptr(status), _stream(stream))
+    _check(code, "sv_tree_expand")

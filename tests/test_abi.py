@@ -122,6 +122,50 @@ def test_loss_host_validation(L):
     assert loss(L, ws=None) == sv.ERR_WORKSPACE
 
 
+def compact(L, **kw):
+    a = dict(B=2, T=4, Hkv=2, D=64, kv_cap=64, dt=sv.BF16, k=FAKE, v=FAKE, kv_len=FAKE, par=FAKE, al=FAKE, path=FAKE,
+             nl=C.c_void_p(0x200000), st=None)
+    a.update(kw)
+    return L.sv_kv_compact(a["B"], a["T"], a["Hkv"], a["D"], a["kv_cap"], a["dt"], a["k"], a["v"], a["kv_len"],
+                           a["par"], a["al"], a["path"], a["nl"], a["st"], None)
+
+
+def test_kv_compact_host_validation(L):
+    assert compact(L, T=65) == sv.ERR_TREE_TOO_LARGE
+    assert compact(L, T=0) == sv.ERR_INVALID_ARG
+    assert compact(L, kv_cap=3) == sv.ERR_INVALID_ARG
+    assert compact(L, Hkv=0) == sv.ERR_INVALID_ARG
+    assert compact(L, dt=5) == sv.ERR_UNSUPPORTED
+    assert compact(L, D=12) == sv.ERR_UNSUPPORTED               # 24-byte rows are not 16-byte multiples
+    assert compact(L, D=4096, dt=sv.F32) == sv.ERR_UNSUPPORTED  # rows above 8 KB
+    assert compact(L, path=None) == sv.ERR_INVALID_ARG
+    assert compact(L, nl=FAKE) == sv.ERR_INVALID_ARG            # new_kv_len aliases kv_len
+    assert compact(L, k=ODD) == sv.ERR_UNSUPPORTED
+    assert compact(L, B=0) == sv.OK
+
+
+def expand(L, **kw):
+    a = dict(B=2, NF=4, V=100, k=4, keep=8, dt=sv.BF16, z=FAKE, fs=FAKE, tt=FAKE, tl=FAKE, cp=FAKE, ct=FAKE, cs=FAKE,
+             st=None)
+    a.update(kw)
+    return L.sv_tree_expand(a["B"], a["NF"], a["V"], a["k"], a["keep"], a["dt"], a["z"], a["fs"], a["tt"], a["tl"],
+                            a["cp"], a["ct"], a["cs"], a["st"], None)
+
+
+def test_tree_expand_host_validation(L):
+    assert expand(L, k=0) == sv.ERR_INVALID_ARG
+    assert expand(L, k=17) == sv.ERR_INVALID_ARG                # k above 16
+    assert expand(L, V=3) == sv.ERR_INVALID_ARG                 # k > V
+    assert expand(L, keep=17) == sv.ERR_INVALID_ARG             # more survivors than candidates
+    assert expand(L, NF=300, k=4, keep=1) == sv.ERR_INVALID_ARG # more than 1024 candidates
+    assert expand(L, NF=0) == sv.ERR_INVALID_ARG
+    assert expand(L, dt=sv.E4M3) == sv.ERR_UNSUPPORTED
+    assert expand(L, tt=None) == sv.ERR_INVALID_ARG
+    assert expand(L, cs=None) == sv.ERR_INVALID_ARG
+    assert expand(L, z=ODD) == sv.ERR_UNSUPPORTED
+    assert expand(L, B=0) == sv.OK
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(sv, "_lib", None)
     monkeypatch.setattr(sv, "LIB_PATH", tmp_path / "missing.so")
