@@ -22,6 +22,7 @@
 #include <mutex>
 
 #include "sv_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -69,8 +70,7 @@ __device__ __forceinline__ uint32_t fx_weight(float y, float m) {
     return __float2uint_rd(__fmul_rn(fx_exp2_poly(f), scale));
 }
 
-// ---- the same weight for two tokens at once, with packed f32x2 arithmetic (each lane an IEEE fp32
-// operation with round-to-nearest, so the result is bit for bit the scalar fx_weight's)
+// ---- packed f32x2 helpers (each lane an IEEE fp32 operation rounded to nearest)
 __device__ __forceinline__ u64 f2_pack(float lo, float hi) {
     u64 r;
     asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
@@ -79,16 +79,6 @@ __device__ __forceinline__ u64 f2_pack(float lo, float hi) {
 __device__ __forceinline__ void f2_unpack(u64 v, float& lo, float& hi) {
     asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
 }
-__device__ __forceinline__ u64 f2_mul(u64 a, u64 b) {
-    u64 r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ u64 f2_add(u64 a, u64 b) {
-    u64 r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
 __device__ __forceinline__ u64 f2_fma(u64 a, u64 b, u64 c) {
     u64 r;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
@@ -96,39 +86,17 @@ __device__ __forceinline__ u64 f2_fma(u64 a, u64 b, u64 c) {
 }
 __device__ __forceinline__ u64 f2_splat(float x) { return f2_pack(x, x); }
 
-// weights of the tokens with scaled logits y (packed pair) against the row maximum m (negm2 = -m, packed)
-__device__ __forceinline__ void fx_weight2(u64 y2, u64 negm2, uint32_t& w0, uint32_t& w1) {
-    const u64 t2 = f2_mul(f2_add(y2, negm2), f2_splat(0x1.715476p+0f));
-    const u64 r2 = f2_add(t2, f2_splat(12582912.0f));
-    const u64 nf2 = f2_add(r2, f2_splat(-12582912.0f));
-    const u64 f2 = f2_add(t2, nf2 ^ 0x8000000080000000ull);       // t - rint(t)
-    u64 p = f2_splat(0x1.ffcbfcp-17f);
-    p = f2_fma(p, f2, f2_splat(0x1.430912p-13f));
-    p = f2_fma(p, f2, f2_splat(0x1.5d87fep-10f));
-    p = f2_fma(p, f2, f2_splat(0x1.3b2ab6p-7f));
-    p = f2_fma(p, f2, f2_splat(0x1.c6b08ep-5f));
-    p = f2_fma(p, f2, f2_splat(0x1.ebfbe0p-3f));
-    p = f2_fma(p, f2, f2_splat(0x1.62e430p-1f));
-    p = f2_fma(p, f2, f2_splat(1.0f));
-    const int n0 = (int)(uint32_t)r2 - 0x4B400000, n1 = (int)(uint32_t)(r2 >> 32) - 0x4B400000;
-    const u64 sc2 = ((u64)((uint32_t)(127 + 24 + n1) << 23) << 32) | (u64)((uint32_t)(127 + 24 + n0) << 23);
-    float v0, v1, t0, t1;
-    f2_unpack(f2_mul(p, sc2), v0, v1);
-    f2_unpack(t2, t0, t1);
-    w0 = (t0 >= -24.0f) ? __float2uint_rd(v0) : 0u;   // lanes below -24 are discarded whatever they computed
-    w1 = (t1 >= -24.0f) ? __float2uint_rd(v1) : 0u;
-}
-
 // One rejection step of the residual, exactly in integers:
 //   floor(max(0, w * d - wq * X) / d)  =  max(0, w - ceil(wq * X / d)),
-// with X = a * d + b (b < d) and F = floor(2^64 * b / d) prepared once per rejection.  For wq <= 2^25,
-// floor(wq * b / d) is umulhi(wq, F) or one more, decided by an exact 128-bit product; no division and no
-// double precision per token.
+// with X = a * d + b (b < d) and F = floor(2^64 * b / d) prepared once per rejection.  For wq < 2^32,
+// q0 = floor(wq * F / 2^64) is floor(wq * b / d) or one less (wq * F / 2^64 is below wq * b / d by less
+// than wq / 2^64 < 1), so r0 = wq * b - q0 * d lies in [0, 2d) and, for d <= 2^63, is exact in 64-bit
+// wrapping arithmetic; r0 >= d decides the last unit and r0 mod d == 0 tells an exact quotient.
 struct ResidStep {
     u64 a, b, F;
 };
 
-// floor(2^64 * b / d) for b < d < 2^62, by restoring division (once per rejection)
+// floor(2^64 * b / d) for b < d < 2^63, by restoring division (once per rejection)
 __device__ u64 frac64(u64 b, u64 d) {
     u64 q = 0, r = b;
     for (int i = 0; i < 64; ++i) {
@@ -142,26 +110,13 @@ __device__ u64 frac64(u64 b, u64 d) {
     return q;
 }
 
-// x * y for x < 2^32 as a 128-bit value, from two 32 x 32 -> 64-bit products
-__device__ __forceinline__ u128 mul_32x64(uint32_t x, u64 y) {
-    return (u128)((u64)x * (uint32_t)y) + ((u128)((u64)x * (uint32_t)(y >> 32)) << 32);
-}
-
 __device__ __forceinline__ u64 resid_step(u64 w, u64 wq64, const ResidStep& k, u64 d) {
-    const uint32_t wq = (uint32_t)wq64;   // a weight: at most 2^24
-    const u64 q0 = (u64)(mul_32x64(wq, k.F) >> 64);
-    const u128 num = mul_32x64(wq, k.b);
-    const u128 m1 = mul_32x64((uint32_t)(q0 + 1), d);
-    u64 q;
-    bool exact;
-    if (num >= m1) {
-        q = q0 + 1;
-        exact = num == m1;
-    } else {
-        q = q0;
-        exact = num == mul_32x64((uint32_t)q0, d);
-    }
-    const u64 c = (u64)wq * k.a + q + (exact ? 0u : 1u);
+    const u64 wq = (uint32_t)wq64;   // a weight: at most 2^24.5
+    const u64 q0 = __umul64hi(wq, k.F);
+    const u64 r0 = wq * k.b - q0 * d;
+    const bool ge = r0 >= d;
+    const u64 rem = ge ? r0 - d : r0;
+    const u64 c = wq * k.a + q0 + (ge ? 1u : 0u) + (rem != 0 ? 1u : 0u);
     return w > c ? w - c : 0u;
 }
 
@@ -290,7 +245,6 @@ __global__ void __launch_bounds__(kRowThreads) accept_rows_kernel(AcceptArgs a, 
     if (STOCH && tot.fin) {
         const float m = tot.ymax;
         if (vec_ok) {
-            const u64 invT2 = f2_splat(invT), negm2 = f2_splat(-m);
 #pragma unroll 2
             for (int k = c0 + tid * VEC; k < c1; k += kRowThreads * VEC) {
                 float z[VEC];
@@ -298,7 +252,8 @@ __global__ void __launch_bounds__(kRowThreads) accept_rows_kernel(AcceptArgs a, 
 #pragma unroll
                 for (int e = 0; e < VEC; e += 2) {
                     uint32_t w0, w1;
-                    fx_weight2(f2_mul(f2_pack(z[e], z[e + 1]), invT2), negm2, w0, w1);
+                    w0 = fx_weight(__fmul_rn(z[e], invT), m);
+                    w1 = fx_weight(__fmul_rn(z[e + 1], invT), m);
                     S += (u64)w0 + w1;
                 }
             }
@@ -329,11 +284,267 @@ __global__ void __launch_bounds__(kRowThreads) accept_rows_kernel(AcceptArgs a, 
         st.zmax = tot.zmax;
         st.arg = zfin_all ? tot.zarg : -1;
         st.ymax = tot.ymax;
-        st.fin = STOCH ? tot.fin : zfin_all;
+        st.fin = STOCH ? (tot.fin ? 2 : 0) : zfin_all;   // 2: finite, range of y not examined
         st.S = STOCH ? tot.S : 0;
         ((RowStat*)a.ws)[row] = st;
         if (a.argmax && !is_draft) a.argmax[r] = st.arg;
     }
+    pdl_launch_dependents();
+}
+
+// ------------------------------------------------------------------------------------ kernel 1b: staged rows
+// Stochastic rows of bf16 logits (rows 16-byte aligned): each CTA of the row's cluster copies its slice
+// into shared memory with bulk copies (kStoPieces pieces, one mbarrier each), so the row is read from HBM
+// once.  Pass 1 takes the max and min of z with packed bf16x2 instructions while the pieces arrive; the
+// cluster agrees on m = fp32(max z * invT); pass 2 computes the fixed-point weights from shared memory.
+//
+// Pass 2 uses two exact identities of the contract's arithmetic:
+//  * the Horner polynomial with every coefficient scaled by 2^24 returns exactly P(f) * 2^24 (scaling by a
+//    power of two commutes with round-to-nearest in the normal range), and that value lies in
+//    [2^23.5, 2^24.5), where every float is an integer;
+//  * floor(x * 2^n) for n <= 0 and an integer x is x >> -n, and x >> s is 0 for s >= 25 > log2(x), so the
+//    t < -24 case needs no test (t in [-24.5, -24) gives P < 1 at n = -24, also 0).
+// The identities need |t| < 2^22 (rint by the 1.5 * 2^23 constant); rows whose range of y is wider take
+// the scalar contract instead.
+constexpr int kStoThreads = 256;
+constexpr int kStoPieces = 4;
+constexpr int kStoMaxSlice = 96 * 1024;   // bytes of shared memory for one CTA's slice
+
+__device__ __forceinline__ uint32_t shr_clamped(uint32_t x, uint32_t s) {   // PTX clamps shifts above 32
+    uint32_t r;
+    asm("shr.b32 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(s));
+    return r;
+}
+__device__ __forceinline__ uint32_t f2u_floor(float x) {
+    uint32_t r;
+    asm("cvt.rmi.u32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+// the contract's weights of two tokens with logits z0, z1 against the row maximum m of y = z * invT, for
+// rows whose every t is above -2^22 (see above); bit for bit fx_weight's.  The rounding steps before the
+// polynomial (y, y - m, t, rint t, f) are scalar round-to-nearest intrinsics, which the compiler never
+// fuses: packed f32x2 multiplies whose product feeds a packed add (also when written as an fma with a unit
+// multiplier) were measured to be fused into one rounding, which moves rint(t) at half-integers.  The
+// polynomial is an explicit fma chain, evaluated on both tokens at once.  UNIT_T: invT == 1, so y = z.
+template <bool UNIT_T>
+__device__ __forceinline__ void fx_weight2_fast(float z0, float z1, float invT, float m, uint32_t& w0, uint32_t& w1) {
+    const float y0 = UNIT_T ? z0 : __fmul_rn(z0, invT), y1 = UNIT_T ? z1 : __fmul_rn(z1, invT);
+    const float t0 = __fmul_rn(__fsub_rn(y0, m), 0x1.715476p+0f);
+    const float t1 = __fmul_rn(__fsub_rn(y1, m), 0x1.715476p+0f);
+    const float r0 = __fadd_rn(t0, 12582912.0f), r1 = __fadd_rn(t1, 12582912.0f);
+    const u64 f2 = f2_pack(__fsub_rn(t0, __fsub_rn(r0, 12582912.0f)), __fsub_rn(t1, __fsub_rn(r1, 12582912.0f)));
+    u64 p = f2_splat(0x1.ffcbfcp-17f * 16777216.0f);
+    p = f2_fma(p, f2, f2_splat(0x1.430912p-13f * 16777216.0f));
+    p = f2_fma(p, f2, f2_splat(0x1.5d87fep-10f * 16777216.0f));
+    p = f2_fma(p, f2, f2_splat(0x1.3b2ab6p-7f * 16777216.0f));
+    p = f2_fma(p, f2, f2_splat(0x1.c6b08ep-5f * 16777216.0f));
+    p = f2_fma(p, f2, f2_splat(0x1.ebfbe0p-3f * 16777216.0f));
+    p = f2_fma(p, f2, f2_splat(0x1.62e430p-1f * 16777216.0f));
+    p = f2_fma(p, f2, f2_splat(16777216.0f));
+    float p0, p1;
+    f2_unpack(p, p0, p1);
+    w0 = shr_clamped(f2u_floor(p0), 0x4B400000u - __float_as_uint(r0));   // shift by -rint(t)
+    w1 = shr_clamped(f2u_floor(p1), 0x4B400000u - __float_as_uint(r1));
+}
+
+// the sum of the weights of the two bf16 logits packed in `w` (fast-path rows)
+template <bool UNIT_T>
+__device__ __forceinline__ uint32_t fx_weight_pair_fast(uint32_t w, float invT, float m) {
+    uint32_t w0, w1;
+    fx_weight2_fast<UNIT_T>(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u), invT, m, w0, w1);
+    return w0 + w1;
+}
+
+template <bool WANT_ARG>
+__global__ void __launch_bounds__(kStoThreads) accept_rows_staged_kernel(AcceptArgs a, int CL, int chunk,
+                                                                          int rows_src) {
+    cg::cluster_group cluster = cg::this_cluster();
+    extern __shared__ __align__(128) unsigned char s_dyn[];
+    __shared__ __align__(8) uint64_t s_bar[kStoPieces];
+    __shared__ float s_red[2][kStoThreads / 32];
+    __shared__ int s_redi[kStoThreads / 32];
+    __shared__ u64 s_ws[kStoThreads / 32];
+    __shared__ float s_zmax, s_zmin;
+    __shared__ int s_arg;
+    __shared__ u64 s_S;
+    __shared__ int s_err;
+
+    const int rank = (int)cluster.block_rank();
+    const int row = blockIdx.x / CL;
+    const bool is_draft = row >= rows_src;
+    const int r = is_draft ? row - rows_src : row;
+    const int V = a.V;
+    const uint16_t* base = (const uint16_t*)(is_draft ? a.draft : a.target) + (size_t)r * V;
+    const int c0 = min(V, rank * chunk), c1 = min(V, c0 + chunk);
+    const int nvec = (c1 - c0) / 8;                    // whole 16-byte vectors (V % 8 == 0)
+    const int per = (nvec + kStoPieces - 1) / kStoPieces;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint4* sv4 = reinterpret_cast<const uint4*>(s_dyn);
+
+    if (tid == 0) {
+        s_err = 0;
+        for (int q = 0; q < kStoPieces; ++q) tc::mbar_init(&s_bar[q], 1);
+        tc::mbar_fence_init();
+        for (int q = 0; q < kStoPieces; ++q) {
+            const int v0 = min(nvec, q * per), v1 = min(nvec, v0 + per);
+            const uint32_t bytes = (uint32_t)(v1 - v0) * 16u;
+            tc::mbar_arrive_expect_tx(&s_bar[q], bytes);
+            if (bytes) tc::bulk_g2s(s_dyn + (size_t)v0 * 16, base + c0 + (size_t)v0 * 8, bytes, &s_bar[q]);
+        }
+    }
+    __syncthreads();
+
+    // pass 1: max and min of z (NaN propagates through max.NaN / min.NaN, infinities become the extremes)
+    __nv_bfloat162 mx2 = __halves2bfloat162(__ushort_as_bfloat16(0xff80), __ushort_as_bfloat16(0xff80));   // -inf
+    __nv_bfloat162 mn2 = __halves2bfloat162(__ushort_as_bfloat16(0x7f80), __ushort_as_bfloat16(0x7f80));   // +inf
+    bool ok = true;
+    for (int q = 0; q < kStoPieces; ++q) {
+        ok = ok && tc::mbar_wait(&s_bar[q], 0, &s_err);
+        if (!ok) break;
+        const int v0 = min(nvec, q * per), v1 = min(nvec, v0 + per);
+#pragma unroll 4
+        for (int v = v0 + tid; v < v1; v += kStoThreads) {
+            const uint4 x = sv4[v];
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
+                mx2 = __hmax2_nan(mx2, h);
+                mn2 = __hmin2_nan(mn2, h);
+            }
+        }
+    }
+    float zmax = fmaxf(__low2float(mx2), __high2float(mx2));
+    float zmin = fminf(__low2float(mn2), __high2float(mn2));
+    if (isnan(__low2float(mx2)) || isnan(__high2float(mx2))) zmax = __int_as_float(0x7fc00000);
+    // block and cluster: NaN-propagating max / min
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, zmax, o), n2 = __shfl_xor_sync(0xffffffffu, zmin, o);
+        zmax = (isnan(zmax) || isnan(m2)) ? __int_as_float(0x7fc00000) : fmaxf(zmax, m2);
+        zmin = fminf(zmin, n2);
+    }
+    if (lane == 0) { s_red[0][warp] = zmax; s_red[1][warp] = zmin; }
+    __syncthreads();
+    if (tid == 0) {
+        for (int w = 1; w < kStoThreads / 32; ++w) {
+            zmax = (isnan(zmax) || isnan(s_red[0][w])) ? __int_as_float(0x7fc00000) : fmaxf(zmax, s_red[0][w]);
+            zmin = fminf(zmin, s_red[1][w]);
+        }
+        s_zmax = zmax;
+        s_zmin = zmin;
+    }
+    cluster.sync();
+    zmax = *cluster.map_shared_rank(&s_zmax, 0);
+    zmin = *cluster.map_shared_rank(&s_zmin, 0);
+    int err = *cluster.map_shared_rank(&s_err, 0);
+    for (int q = 1; q < CL; ++q) {
+        const float m2 = *cluster.map_shared_rank(&s_zmax, q);
+        zmax = (isnan(zmax) || isnan(m2)) ? __int_as_float(0x7fc00000) : fmaxf(zmax, m2);
+        zmin = fminf(zmin, *cluster.map_shared_rank(&s_zmin, q));
+        err |= *cluster.map_shared_rank(&s_err, q);
+    }
+    cluster.sync();   // partials consumed
+
+    // every z finite iff max and min are; every y finite iff the two extremes of y are (y monotone in z)
+    const float invT = a.invT;
+    const bool zfin = isfinite(zmax) && isfinite(zmin);
+    const float m = __fmul_rn(zmax, invT);
+    const float ymin = __fmul_rn(zmin, invT);
+    const bool yfin = zfin && isfinite(m) && isfinite(ymin);
+    u64 S = 0;
+    int arg = 0x7fffffff;
+    const bool fast_row = yfin && __fsub_rn(m, ymin) < 2097152.0f;    // every |t| < 1.45 * 2^21 < 2^22
+    if (yfin && !err) {
+        const bool fast = fast_row;
+        const uint32_t zmax_bits = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(zmax));
+        const uint32_t zmax2 = zmax_bits | (zmax_bits << 16);
+        const bool unit_t = invT == 1.0f;
+        if (fast) {
+#pragma unroll 2
+            for (int v = tid; v < nvec; v += kStoThreads) {
+                const uint4 x = sv4[v];
+                uint32_t acc;
+                if (unit_t) {
+                    acc = fx_weight_pair_fast<true>(x.x, invT, m) + fx_weight_pair_fast<true>(x.y, invT, m) +
+                          fx_weight_pair_fast<true>(x.z, invT, m) + fx_weight_pair_fast<true>(x.w, invT, m);
+                } else {
+                    acc = fx_weight_pair_fast<false>(x.x, invT, m) + fx_weight_pair_fast<false>(x.y, invT, m) +
+                          fx_weight_pair_fast<false>(x.z, invT, m) + fx_weight_pair_fast<false>(x.w, invT, m);
+                }
+                S += acc;
+                if (WANT_ARG && arg == 0x7fffffff) {
+                    const __nv_bfloat162 m2 = *reinterpret_cast<const __nv_bfloat162*>(&zmax2);
+                    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+                    uint32_t eq = 0;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) eq |= __heq2_mask(*reinterpret_cast<const __nv_bfloat162*>(&w[e]), m2);
+                    if (eq) {
+                        for (int e = 0; e < 8 && arg == 0x7fffffff; ++e)
+                            if (__uint_as_float(e & 1 ? (w[e >> 1] & 0xffff0000u) : (w[e >> 1] << 16)) == zmax)
+                                arg = c0 + v * 8 + e;
+                    }
+                }
+            }
+        } else {
+            for (int v = tid; v < nvec; v += kStoThreads) {
+                const uint4 x = sv4[v];
+                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float z = __uint_as_float(e & 1 ? (w[e >> 1] & 0xffff0000u) : (w[e >> 1] << 16));
+                    S += fx_weight(__fmul_rn(z, invT), m);
+                    if (WANT_ARG && z == zmax && arg == 0x7fffffff) arg = c0 + v * 8 + e;
+                }
+            }
+        }
+    } else if (WANT_ARG && zfin && !err) {
+        // y overflowed but z is finite: the argmax is still defined
+        for (int v = tid; v < nvec && arg == 0x7fffffff; v += kStoThreads) {
+            const uint4 x = sv4[v];
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+            for (int e = 0; e < 8 && arg == 0x7fffffff; ++e)
+                if (__uint_as_float(e & 1 ? (w[e >> 1] & 0xffff0000u) : (w[e >> 1] << 16)) == zmax) arg = c0 + v * 8 + e;
+        }
+    }
+    S = warp_sum_u64(S);
+    if (WANT_ARG) {
+#pragma unroll
+        for (int o = 16; o; o >>= 1) arg = min(arg, __shfl_xor_sync(0xffffffffu, arg, o));
+    }
+    if (lane == 0) { s_ws[warp] = S; s_redi[warp] = arg; }
+    __syncthreads();
+    if (tid == 0) {
+        u64 t = 0;
+        int am = 0x7fffffff;
+        for (int w = 0; w < kStoThreads / 32; ++w) { t += s_ws[w]; am = min(am, s_redi[w]); }
+        s_S = t;
+        s_arg = am;
+    }
+    cluster.sync();
+    if (rank == 0 && tid == 0) {
+        u64 t = 0;
+        int am = 0x7fffffff;
+        for (int q = 0; q < CL; ++q) {
+            t += *cluster.map_shared_rank(&s_S, q);
+            am = min(am, *cluster.map_shared_rank(&s_arg, q));
+        }
+        RowStat st;
+        st.zmax = zmax;
+        st.arg = (zfin && !err) ? am : -1;
+        st.ymax = m;
+        st.fin = err ? -1 : (yfin ? (fast_row ? 1 : 2) : 0);   // 1: finite with every t above -2^22
+        st.S = (yfin && !err) ? t : 0;
+        ((RowStat*)a.ws)[row] = st;
+        if (a.argmax && !is_draft) a.argmax[r] = st.arg;
+    }
+    if (err && tid == 0) {
+        // give the copies still in flight a bounded chance to land before the shared memory is released
+        int e2 = 0;
+        for (int q = 0; q < kStoPieces; ++q) tc::mbar_wait(&s_bar[q], 0, &e2);
+    }
+    cluster.sync();   // keep every CTA's shared memory alive until CTA 0 has read it
     pdl_launch_dependents();
 }
 
@@ -379,14 +590,20 @@ __global__ void __launch_bounds__(kWalkThreads, 2) accept_walk_kernel(AcceptArgs
     for (int c = 1 + tid; c < T; c += kWalkThreads) bad |= (sh.tok[c] < 0 || sh.tok[c] >= V);
     if (__syncthreads_or(bad) && st == SV_OK) st = SV_ERR_INVALID_ARG;
     if (st == SV_OK) {
-        int nf = 0;
+        int nf = 0, to = 0;
         for (int r = tid; r < T; r += kWalkThreads) {
             const RowStat rs = stats[(size_t)b * T + r];
             nf |= !rs.fin;
+            to |= rs.fin < 0;
             if (MODE == MODE_GREEDY) sh.arg[r] = rs.arg;
-            if (MODE == MODE_PROB) nf |= !stats[(size_t)B * T + (size_t)b * T + r].fin;
+            if (MODE == MODE_PROB) {
+                const int fq = stats[(size_t)B * T + (size_t)b * T + r].fin;
+                nf |= !fq;
+                to |= fq < 0;
+            }
         }
-        if (__syncthreads_or(nf)) st = SV_ERR_NONFINITE;
+        if (__syncthreads_or(to)) st = SV_ERR_TIMEOUT;
+        else if (__syncthreads_or(nf)) st = SV_ERR_NONFINITE;
     }
     const bool writer = rank == 0 && tid == 0;
     if (st != SV_OK) {
@@ -457,8 +674,10 @@ __global__ void __launch_bounds__(kWalkThreads, 2) accept_walk_kernel(AcceptArgs
                 return wres_z(LG::load(prow_p + k), MODE == MODE_PROB ? LG::load(prow_q + k) : 0.f, k);
             };
             // the VEC residual weights of tokens k .. k+VEC-1 (16-byte loads; rows are 16-byte aligned)
-            const u64 invT2 = f2_splat(invT), negmp2 = f2_splat(-sp.ymax);
-            const u64 negmq2 = f2_splat(MODE == MODE_PROB ? -sq.ymax : 0.f);
+            // rows marked by the staged row kernel as having every t above -2^22 take the shift form of the
+            // weights (identical integers, fewer instructions)
+            const bool fastp = sp.fin == 1;
+            const bool fastq = MODE == MODE_PROB ? sq.fin == 1 : true;
             auto wres_vec = [&](int k, u64 (&w)[VEC]) {
                 float zp[VEC], zq[VEC];
                 LG::load_vec(prow_p + k, zp);
@@ -466,7 +685,8 @@ __global__ void __launch_bounds__(kWalkThreads, 2) accept_walk_kernel(AcceptArgs
 #pragma unroll
                 for (int e = 0; e < VEC; e += 2) {
                     uint32_t p0, p1;
-                    fx_weight2(f2_mul(f2_pack(zp[e], zp[e + 1]), invT2), negmp2, p0, p1);
+                    if (fastp) fx_weight2_fast<false>(zp[e], zp[e + 1], invT, sp.ymax, p0, p1);
+                    else { p0 = fx_weight(__fmul_rn(zp[e], invT), sp.ymax); p1 = fx_weight(__fmul_rn(zp[e + 1], invT), sp.ymax); }
                     w[e] = p0;
                     w[e + 1] = p1;
                     if (MODE == MODE_ONEHOT) {
@@ -476,7 +696,8 @@ __global__ void __launch_bounds__(kWalkThreads, 2) accept_walk_kernel(AcceptArgs
                         }
                     } else if (MODE == MODE_PROB && nrej) {
                         uint32_t q0, q1;
-                        fx_weight2(f2_mul(f2_pack(zq[e], zq[e + 1]), invT2), negmq2, q0, q1);
+                        if (fastq) fx_weight2_fast<false>(zq[e], zq[e + 1], invT, sq.ymax, q0, q1);
+                        else { q0 = fx_weight(__fmul_rn(zq[e], invT), sq.ymax); q1 = fx_weight(__fmul_rn(zq[e + 1], invT), sq.ymax); }
                         for (int i = 0; i < nrej; ++i) {
                             w[e] = resid_step(w[e], q0, sh.rs[i], Sq);
                             w[e + 1] = resid_step(w[e + 1], q1, sh.rs[i], Sq);
@@ -682,7 +903,27 @@ cudaError_t launch_typed(const AcceptArgs& a, cudaStream_t s) {
     int chunk = (a.V + CL - 1) / CL;
     chunk = (chunk + VEC - 1) / VEC * VEC;
     cudaError_t e;
-    if (stoch) e = launch_ex(accept_rows_kernel<LDT, true>, dim3(CL * rows), dim3(kRowThreads), 0, s, CL, false, a, CL, chunk, rows_src);
+    // Stochastic bf16 rows whose slices fit in shared memory: the staged kernel (one HBM read per row).
+    // The cluster is the smallest power of two that keeps a slice within about 40 KB (several CTAs per SM).
+    int CLs = 1;
+    const long long row_bytes = (long long)a.V * 2;
+    while (CLs < kMaxCluster && row_bytes > (long long)CLs * 40 * 1024) CLs *= 2;
+    int chunk_s = ((a.V + CLs - 1) / CLs + 7) / 8 * 8;
+    const bool staged = stoch && LDT == SV_BF16 && a.V % 8 == 0 && (long long)chunk_s * 2 <= kStoMaxSlice;
+    if (staged) {
+        const size_t smem = (size_t)chunk_s * 2;
+        static bool attr_set[2] = {false, false};
+        if (!attr_set[a.argmax ? 1 : 0]) {
+            // room for the slice, and the whole unified L1 as shared memory so several CTAs fit on an SM
+            const void* fn = a.argmax ? (const void*)accept_rows_staged_kernel<true> : (const void*)accept_rows_staged_kernel<false>;
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kStoMaxSlice);
+            if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+            if (e != cudaSuccess) return e;
+            attr_set[a.argmax ? 1 : 0] = true;
+        }
+        if (a.argmax) e = launch_ex(accept_rows_staged_kernel<true>, dim3(CLs * rows), dim3(kStoThreads), smem, s, CLs, false, a, CLs, chunk_s, rows_src);
+        else          e = launch_ex(accept_rows_staged_kernel<false>, dim3(CLs * rows), dim3(kStoThreads), smem, s, CLs, false, a, CLs, chunk_s, rows_src);
+    } else if (stoch) e = launch_ex(accept_rows_kernel<LDT, true>, dim3(CL * rows), dim3(kRowThreads), 0, s, CL, false, a, CL, chunk, rows_src);
     else       e = launch_ex(accept_rows_kernel<LDT, false>, dim3(CL * rows), dim3(kRowThreads), 0, s, CL, false, a, CL, chunk, rows_src);
     if (e != cudaSuccess) return e;
     const int CLW = (mode == MODE_GREEDY) ? 1 : pick_cluster(a.V, kWalkThreads * 8);

@@ -73,6 +73,7 @@ __global__ void kv_compact_kernel(CompactArgs a, int chunks) {
 // ------------------------------------------------------------------------------------ tree expansion
 constexpr int kExpThreads = 256;
 constexpr int kExpMaxCluster = 8;
+constexpr int kExpBatch = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -189,25 +190,33 @@ __global__ void __launch_bounds__(kExpThreads) expand_rows_kernel(ExpandArgs a, 
     int fin = 1;
     const bool vec_ok = (V % VEC) == 0;
     if (vec_ok) {
-#pragma unroll 2
-        for (int kb = c0 + tid * VEC; kb < c1; kb += kExpThreads * VEC) {
-            float z[VEC];
-            RW::load_vec(base + kb, z);
-            float mx = m;
+        // kExpBatch vectors a thread, all loads issued before any is used; elements still reach the top-k
+        // lists in increasing index order
+        constexpr int STRIDE = kExpThreads * VEC;
+        for (int kb = c0 + tid * VEC; kb < c1; kb += kExpBatch * STRIDE) {
+            float z[kExpBatch][VEC];
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                fin &= fabsf(z[e]) <= 3.402823466e38f;
-                mx = fmaxf(mx, z[e]);
+            for (int u = 0; u < kExpBatch; ++u)
+                if (kb + u * STRIDE < c1) RW::load_vec(base + kb + u * STRIDE, z[u]);
+#pragma unroll
+            for (int u = 0; u < kExpBatch; ++u) {
+                if (kb + u * STRIDE >= c1) break;
+                float mx = m;
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    fin &= fabsf(z[u][e]) <= 3.402823466e38f;
+                    mx = fmaxf(mx, z[u][e]);
+                }
+                if (mx > m) {   // rescale the running sum to the new maximum
+                    s *= ex2_approx((m - mx) * kLog2e);
+                    m = mx;
+                }
+                const float ml = m * kLog2e;
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) s += ex2_approx(__fmaf_rn(z[u][e], kLog2e, -ml));
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) tk.push(z[u][e], kb + u * STRIDE + e);
             }
-            if (mx > m) {   // rescale the running sum to the new maximum
-                s *= ex2_approx((m - mx) * kLog2e);
-                m = mx;
-            }
-            const float ml = m * kLog2e;
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) s += ex2_approx(__fmaf_rn(z[e], kLog2e, -ml));
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) tk.push(z[e], kb + e);
         }
     } else {
         for (int kk = c0 + tid; kk < c1; kk += kExpThreads) {

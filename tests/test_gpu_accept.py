@@ -107,3 +107,94 @@ def test_fp8_long_context_accept_full_size(temp):
                         temperature=temp)
     g = check(w, temperature=temp, draft=None)
     assert (g["status"] == 0).all()
+
+
+def check_opts(w, temperature, draft, want_argmax):
+    ref = oracle.accept(w.target_logits, w.tokens, w.parent, V=w.V, logit_dt=w.logit_dt, temperature=temperature,
+                        draft=draft, uniforms=w.uniforms, want_argmax=want_argmax)
+    got = run_accept(w.target_logits, w.tokens, w.parent, V=w.V, temperature=temperature, draft=draft,
+                     uniforms=w.uniforms, want_argmax=want_argmax)
+    compare(got, ref)
+    return got
+
+
+@pytest.mark.parametrize("want_argmax", [False, True])
+@pytest.mark.parametrize("mode", ["prob", "onehot"])
+@pytest.mark.parametrize("V", [1000, 50000, 1001, 40003])
+def test_stochastic_bf16_with_and_without_argmax(want_argmax, mode, V):
+    """bf16 rows whose length keeps them 16-byte aligned take the shared-memory staged kernel (with or
+    without the argmax output); other lengths take the generic kernel."""
+    w = W.make_verify(V + 3, B=17, T=13, Hq=1, Hkv=1, D=8, L=(0, 0), V=V, logit_dt="bf16", tree=(3, 2, 2),
+                      mode=mode, temperature=0.8, force_p=0.7, sigma=2.5, with_attn=False)
+    g = check_opts(w, 0.8, w.draft_logits if mode == "prob" else None, want_argmax)
+    assert (g["status"] == 0).all()
+
+
+def test_stochastic_rows_with_a_very_wide_logit_range():
+    """Rows holding a logit about 4e6 below the rest (|t| beyond 2^21) take the scalar contract path of the
+    staged kernel; the results must not change."""
+    w = W.make_verify(21, B=9, T=6, Hq=1, Hkv=1, D=8, L=(0, 0), V=4096, logit_dt="bf16", tree="chain", mode="prob",
+                      temperature=1.0, sigma=2.5, with_attn=False)
+    w.target_logits = w.target_logits.copy()
+    w.draft_logits = w.draft_logits.copy()
+    low = W.f32_to_bf16(np.float32(-4.0e6))
+    w.target_logits[::2, :, 17] = low
+    w.draft_logits[1::3, :, 4000] = low
+    for want in (False, True):
+        g = check_opts(w, 1.0, w.draft_logits, want)
+        assert (g["status"] == 0).all()
+
+
+def test_stochastic_bf16_status_codes_and_overflow():
+    """NaN and infinite bf16 logits, and finite logits whose y = z / temperature overflows: the request fails
+    with SV_ERR_NONFINITE, while the argmax of a finite row is still reported."""
+    w = W.make_verify(8, B=5, T=6, Hq=1, Hkv=1, D=8, L=(0, 0), V=2048, logit_dt="bf16", tree="chain", mode="onehot",
+                      temperature=0.05, sigma=2.0, with_attn=False)
+    w.target_logits = w.target_logits.copy()
+    w.target_logits[1, 3, 100] = 0x7FC0                     # NaN
+    w.target_logits[2, 0, 5] = 0xFF80                       # -inf
+    w.target_logits[3, 5, 2047] = W.f32_to_bf16(np.float32(3.0e37))[0]   # y = 6e38 overflows float32
+    g = check_opts(w, 0.05, None, True)
+    assert list(g["status"]) == [0, 5, 5, 5, 0]
+    assert g["argmax"][3, 5] == 2047 and g["argmax"][1, 3] == -1
+
+
+def boundary_uniforms(w, temperature, seed, wide_rows=()):
+    """Slot-0 uniform of every request placed at a prefix-sum boundary of the row its bonus is drawn from
+    (T = 1: the root's row, R = S): alternately just below and exactly at cs[j] * 2^32 / S for a token j in
+    the upper half of the mass.  An error of one unit in S moves the threshold across the boundary, and an
+    error in any weight before j moves the prefix sum; either changes the drawn token."""
+    rng = np.random.default_rng(seed)
+    invT = np.float32(1.0 / np.float64(temperature))
+    u = np.zeros((w.B, 1), np.uint32)
+    for b in range(w.B):
+        z = W.decode_f32(w.target_logits[b, 0], w.logit_dt)
+        y = (z * invT).astype(np.float32)
+        wts = oracle.fx_weight(y, float(y.max())).astype(np.uint64)
+        S = int(wts.sum())
+        cs = np.cumsum(wts)
+        cand = np.nonzero((wts > 0) & (cs * 2 >= S) & (cs < S))[0]
+        j = int(rng.choice(cand))
+        up = -(-(int(cs[j]) << 32) // S)               # ceil(cs[j] * 2^32 / S)
+        u[b, 0] = up - 1 if b % 2 == 0 else up
+        assert 0 < u[b, 0] < 2 ** 32
+    return u
+
+
+@pytest.mark.parametrize("V,dt,temp,mode", [(151936, "bf16", 1.0, "prob"), (151936, "bf16", 0.7, "onehot"),
+                                            (50000, "bf16", 0.8, "onehot"), (4096, "f32", 0.7, "onehot"),
+                                            (40003, "bf16", 1.0, "onehot"), (128256, "bf16", 0.3, "onehot")])
+def test_bonus_draw_at_prefix_boundaries_checks_every_weight(V, dt, temp, mode):
+    """Single-node trees: the walk stops at the root at once and draws the bonus from the root's row with
+    R = S, so the drawn token pins the row's weight sum and the prefix sums to the unit."""
+    w = W.make_verify(V + 77, B=48, T=1, Hq=1, Hkv=1, D=8, L=(0, 0), V=V, logit_dt=dt, tree="chain",
+                      mode="prob" if mode == "prob" else "onehot", temperature=temp, sigma=2.5, with_attn=False)
+    if mode == "prob":
+        w.draft_logits = w.draft_logits.copy()
+    w.target_logits = w.target_logits.copy()
+    low = W.f32_to_bf16(np.float32(-4.0e6)) if dt == "bf16" else np.float32(-4.0e6)
+    w.target_logits[1::4, 0, 3] = low                  # a quarter of the rows span more than 2^21 in y
+    w.uniforms = boundary_uniforms(w, temp, V)
+    for want in (False, True):
+        g = check_opts(w, temp, w.draft_logits if mode == "prob" else None, want)
+        assert (g["status"] == 0).all() and (g["accept_len"] == 0).all()
