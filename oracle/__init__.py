@@ -80,6 +80,7 @@ def load(path):
     L.or_loss.argtypes = [i, i, i, P] + [P] * 9
     L.or_kv_compact.argtypes = [i, i, i, i, i, i, P, P, P, P, P, P, P, P]
     L.or_tree_expand.argtypes = [i, i, i, i, i, i, P, P, P, P, P, P, P, P]
+    L.or_tree_attn_bwd.argtypes = [i, i, i, i, i, i, i, i, P, P, P, P, P, C.c_double, P, P, P, P, P]
     return L
 
 
@@ -134,6 +135,26 @@ def tree_attn_w(w, rows=None, sm_scale=0.0):
     """tree_attn on a workloads.Verify batch."""
     return tree_attn(w.q, w.k, w.v, w.kv_len, w.parent, Hq=w.Hq, Hkv=w.Hkv, q_dt=w.q_dt, kv_dt=w.kv_dt,
                      k_scale=w.k_scale, v_scale=w.v_scale, sm_scale=sm_scale, rows=rows)
+
+
+def tree_attn_bwd(q, k, v, kv_len, parent, dout, *, Hq, Hkv, q_dt, kv_dt, sm_scale=0.0):
+    """float64 backward of the tree-masked attention for the upstream gradient dout (q's layout and dtype).
+    Returns (dq [B,T,Hq,D], dk [B,Hkv,kv_cap,D], dv [B,Hkv,kv_cap,D], status [B], rc)."""
+    q = np.ascontiguousarray(q)
+    k = np.ascontiguousarray(k)
+    v = np.ascontiguousarray(v)
+    dout = np.ascontiguousarray(dout)
+    B, T = parent.shape
+    D = q.shape[-1]
+    kv_cap = k.shape[2]
+    dq = np.zeros((B, T, Hq, D))
+    dk = np.zeros((B, Hkv, kv_cap, D))
+    dv = np.zeros((B, Hkv, kv_cap, D))
+    status = np.zeros(B, np.int32)
+    rc = lib().or_tree_attn_bwd(B, T, Hq, Hkv, D, kv_cap, DT[q_dt], DT[kv_dt], _p(q), _p(k), _p(v),
+                                _p(np.ascontiguousarray(kv_len, np.int32)), _p(np.ascontiguousarray(parent, np.int32)),
+                                float(sm_scale), _p(dout), _p(dq), _p(dk), _p(dv), _p(status))
+    return dq, dk, dv, status, rc
 
 
 # ------------------------------------------------------------------------------------------------ acceptance

@@ -622,3 +622,94 @@ int or_tree_expand(int B, int n_front, int V, int k, int n_keep, int logit_dt, c
     }
     return OK;
 }
+
+/* ---------------------------------------------------------------------------------------------- */
+/* tree-masked attention backward (plain definition, float64)                                      */
+/* ---------------------------------------------------------------------------------------------- */
+/* The draft is trained on every accepted and rejected branch of its trees in one batched forward and
+ * backward pass ("Aurora" post, section 2), so the attention of that pass needs its gradient under the
+ * same tree mask.  With p = softmax(s), s_j = scale * <q, k_j> over the allowed set A(b, i) of the forward
+ * (prefix plus the node's ancestors), o = sum_j p_j v_j and an upstream gradient dO = d loss / d o:
+ *     dv_j += p_j dO                      dp_j = <dO, v_j>        delta = <dO, o> = sum_j p_j dp_j
+ *     ds_j  = p_j (dp_j - delta)          dq    = scale * sum_j ds_j k_j
+ *     dk_j += scale * ds_j q
+ * summed over every (node, query head) whose allowed set holds position j.  This is the chain rule of the
+ * softmax written out; the forward (p, o) is recomputed here in float64 from q, k, v.  dq is [B,T,Hq,D];
+ * dk and dv are [B,Hkv,kv_cap,D] with every position outside [0, kv_len + T) left at zero.  E4M3 caches
+ * are not taken (the backward trains a draft whose cache is bf16 or fp32). */
+static void attn_row_bwd(int T, int Hq, int Hkv, int D, int kv_cap, int q_dt, int kv_dt, const void* q,
+                         const void* k, const void* v, const void* dout, int L, const int32_t* par,
+                         double scale, int b, int i, int h, double* dq, double* dk, double* dv) {
+    int G = Hq / Hkv, hk = h / G;
+    int on[64];
+    memset(on, 0, sizeof on);
+    for (int a = i; a >= 0; a = par[a]) on[a] = 1;
+    size_t qoff = (((size_t)b * T + i) * Hq + h) * D;
+    size_t kvbase = ((size_t)b * Hkv + hk) * (size_t)kv_cap * D;
+    int npos = L + T;
+    double* s = (double*)malloc(sizeof(double) * (size_t)npos);
+    double* qv = (double*)malloc(sizeof(double) * (size_t)D);
+    double* g = (double*)malloc(sizeof(double) * (size_t)D);
+    double* o = (double*)calloc((size_t)D, sizeof(double));
+    for (int d = 0; d < D; ++d) { qv[d] = load_elem(q, qoff + d, q_dt); g[d] = load_elem(dout, qoff + d, q_dt); }
+    double m = -INFINITY;
+    for (int j = 0; j < npos; ++j) {
+        if (!(j < L || on[j - L])) { s[j] = -INFINITY; continue; }
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d) acc += qv[d] * load_elem(k, kvbase + (size_t)j * D + d, kv_dt);
+        s[j] = scale * acc;
+        if (s[j] > m) m = s[j];
+    }
+    double sum = 0.0;
+    for (int j = 0; j < npos; ++j) if (s[j] != -INFINITY) sum += exp(s[j] - m);
+    for (int j = 0; j < npos; ++j) {                     /* s becomes p */
+        s[j] = s[j] == -INFINITY ? 0.0 : exp(s[j] - m) / sum;
+        if (s[j] == 0.0) continue;
+        for (int d = 0; d < D; ++d) o[d] += s[j] * load_elem(v, kvbase + (size_t)j * D + d, kv_dt);
+    }
+    double delta = 0.0;
+    for (int d = 0; d < D; ++d) delta += g[d] * o[d];
+    for (int d = 0; d < D; ++d) dq[d] = 0.0;
+    for (int j = 0; j < npos; ++j) {
+        if (!(j < L || on[j - L])) continue;
+        double p = s[j], dp = 0.0;
+        for (int d = 0; d < D; ++d) dp += g[d] * load_elem(v, kvbase + (size_t)j * D + d, kv_dt);
+        double ds = p * (dp - delta);
+        size_t row = ((size_t)b * Hkv + hk) * (size_t)kv_cap + (size_t)j;
+        for (int d = 0; d < D; ++d) {
+            dq[d] += scale * ds * load_elem(k, kvbase + (size_t)j * D + d, kv_dt);
+            dk[row * D + d] += scale * ds * qv[d];
+            dv[row * D + d] += p * g[d];
+        }
+    }
+    free(o); free(g); free(qv); free(s);
+}
+
+int or_tree_attn_bwd(int B, int T, int Hq, int Hkv, int D, int kv_cap, int q_dt, int kv_dt, const void* q,
+                     const void* k, const void* v, const int32_t* kv_len, const int32_t* parent, double sm_scale,
+                     const void* dout, double* dq, double* dk, double* dv, int32_t* status) {
+    if (B < 0 || T < 1 || Hq < 1 || Hkv < 1 || D < 1 || kv_cap < 0) return E_ARG;
+    if (T > 64) return E_BIG;
+    if (Hq % Hkv) return E_ARG;
+    if (q_dt == DT_E4M3 || q_dt < 0 || q_dt > 2 || kv_dt < 0 || kv_dt > 1) return E_UNSUP;
+    double scale = sm_scale != 0.0 ? sm_scale : 1.0 / sqrt((double)D);
+    memset(dk, 0, sizeof(double) * (size_t)B * Hkv * kv_cap * D);
+    memset(dv, 0, sizeof(double) * (size_t)B * Hkv * kv_cap * D);
+    for (int b = 0; b < B; ++b) {
+        int st = or_tree_check(T, parent + (size_t)b * T);
+        if (!st && (kv_len[b] < 0 || kv_len[b] + T > kv_cap)) st = E_ARG;
+        status[b] = st;
+    }
+    /* one thread per request: dk / dv of different requests never overlap */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        for (int i = 0; i < T; ++i)
+            for (int h = 0; h < Hq; ++h) {
+                double* dqr = dq + (((size_t)b * T + i) * Hq + h) * D;
+                if (status[b]) { for (int d = 0; d < D; ++d) dqr[d] = 0.0; continue; }
+                attn_row_bwd(T, Hq, Hkv, D, kv_cap, q_dt, kv_dt, q, k, v, dout, kv_len[b], parent + (size_t)b * T,
+                             scale, b, i, h, dqr, dk, dv);
+            }
+    }
+    return OK;
+}

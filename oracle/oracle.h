@@ -69,6 +69,12 @@ int or_tree_expand(int B, int n_front, int V, int k, int n_keep, int logit_dt, c
                    const float* front_score, int32_t* topk_token, double* topk_logprob, int32_t* child_parent,
                    int32_t* child_token, double* child_score, int32_t* status);
 
+/* Backward of the tree-masked attention, float64: dq [B,T,Hq,D], dk / dv [B,Hkv,kv_cap,D] (zero outside
+ * [0, kv_len + T)) for the upstream gradient dout [B,T,Hq,D] (in q_dt).  kv_dt f32 or bf16. */
+int or_tree_attn_bwd(int B, int T, int Hq, int Hkv, int D, int kv_cap, int q_dt, int kv_dt, const void* q,
+                     const void* k, const void* v, const int32_t* kv_len, const int32_t* parent, double sm_scale,
+                     const void* dout, double* dq, double* dk, double* dv, int32_t* status);
+
 /* Number of OpenMP threads the oracle will use (1 when built without OpenMP). */
 int or_num_threads(void);
 

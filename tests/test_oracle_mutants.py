@@ -12,6 +12,7 @@ import pytest
 import oracle
 from tests import test_oracle_accept as TA
 from tests import test_oracle_attn as TT
+from tests import test_oracle_attn_bwd as TB
 from tests import test_oracle_compact as TC
 from tests import test_oracle_expand as TE
 from tests import test_oracle_loss as TL
@@ -50,6 +51,12 @@ MUTANTS = {
         "cand[s * k + q].score = (double)front_score[r] + ((double)bz - lse);",
         "cand[s * k + q].score = ((double)bz - lse);",
         lambda: TE.test_selection_equals_brute_force_over_all_children(12, 5, 5)),
+    "attn_bwd_drops_delta": (
+        "double ds = p * (dp - delta);", "double ds = p * dp;",
+        lambda: TB.test_backward_matches_autograd_through_sdpa_with_dense_mask("f32", (3, 2, 2), 13)),
+    "attn_bwd_value_grad_uses_q": (
+        "dv[row * D + d] += p * g[d];", "dv[row * D + d] += p * qv[d];",
+        TB.test_backward_matches_central_finite_differences),
     "fx_poly_drops_cubic": (
         "p = fmaf(p, f, C_P3);", "p = fmaf(p, f, 0.0f);", TA.test_fx_exp2_polynomial_error_bound),
 }
