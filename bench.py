@@ -271,6 +271,38 @@ def run_ops(args):
         fn = lambda: sv.loss(z, tok, par, lab, rl, sums, grad=grad, status=st, workspace=ws)
         report(name, "loss+grad", timed(fn), 2 * N * T * V * 2 + N * T * 16)
 
+    def bwd_case(name, w):
+        """Tree-attention backward (CUDA cores): FLOPs = 10 * D per (query row, allowed position) -- the five
+        products s, dp, dq, dk, dv -- against the FP32 CUDA-core peak (152 SMs x 128 FMA lanes x 2 x 2.07 GHz)."""
+        q, k, v = dev(w.q), dev(w.k), dev(w.v)
+        kl, par = dev(w.kv_len), dev(w.parent)
+        out = torch.empty_like(q)
+        lse = torch.empty((w.B, w.T, w.Hq), dtype=torch.float32, device="cuda")
+        sv.tree_attn(q, k, v, kl, par, out, lse=lse)
+        dout = torch.randn(q.shape, device="cuda", generator=gen).to(torch.bfloat16).view(torch.int16)
+        dq = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+        dk = torch.empty(k.shape, dtype=torch.float32, device="cuda")
+        dv = torch.empty(v.shape, dtype=torch.float32, device="cuda")
+        st = torch.empty((w.B,), **i32)
+        ws = torch.empty(max(sv.workspace_size(sv.OP_TREE_ATTN_BWD, w.B, w.T, w.Hq), 256), dtype=torch.uint8,
+                         device="cuda")
+        fn = lambda: sv.tree_attn_bwd(q, k, v, kl, par, out, lse, dout, dq, dk, dv, status=st, workspace=ws)
+        us = timed(fn, reps=5)
+        def n_ancestors(par, i):          # tree slots node i attends to: itself and its ancestors
+            n = 0
+            while i >= 0:
+                n, i = n + 1, int(par[i])
+            return n
+
+        depth = np.array([[n_ancestors(w.parent[b], i) for i in range(w.T)] for b in range(w.B)])
+        pairs = int(sum(int(w.kv_len[b]) * w.T + int(depth[b].sum()) for b in range(w.B))) * w.Hq
+        flops = 10.0 * w.D * pairs
+        peak_alu = 152 * 128 * 2 * 2.07e9 / 1e12   # TFLOP/s
+        tf = flops / (us * 1e-6) / 1e12
+        print(json.dumps({"workload": name, "op": "tree_attn_bwd", "us": round(us, 1), "TFLOP_s": round(tf, 2),
+                          "frac": round(tf / peak_alu, 3), "bound": "alu", "peak_TFLOP_s": round(peak_alu, 1),
+                          "note": "CUDA cores, fp32; FLOPs = 10*D per (query row, allowed position)"}), flush=True)
+
     def compact_case(name, B, T, Hkv, D, kv_cap, kv_dt, kv_len, parent, seed):
         """KV compaction of random accepted root paths; bytes = the moved rows read once and written once."""
         shape = (B, Hkv, kv_cap, D)
@@ -323,6 +355,8 @@ def run_ops(args):
         w = W.make_workload(name, seed=args.seed)
         attn_case(name, w)
         accept_case(name, w, w.temperature, w.draft_logits if w.temperature > 0 else None)
+        if name in ("llama3_8b_tree", "qwen3_8b_stochastic"):
+            bwd_case(name, w)
         compact_case(name, w.B, w.T, w.Hkv, w.D, w.kv_cap, w.kv_dt, w.kv_len, w.parent, args.seed)
         if name == "llama3_8b_tree":
             expand_case(name, w.B, w.V, W.expansion_levels(60, (4, 3, 2, 2, 1, 1)), 3.0, 200 + args.seed)

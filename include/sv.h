@@ -57,7 +57,7 @@ typedef enum {
 
 typedef enum { SV_F32 = 0, SV_BF16 = 1, SV_E4M3 = 2 } sv_dtype;
 
-typedef enum { SV_OP_TREE_ATTN = 0, SV_OP_ACCEPT = 1, SV_OP_LOSS = 2 } sv_op;
+typedef enum { SV_OP_TREE_ATTN = 0, SV_OP_ACCEPT = 1, SV_OP_LOSS = 2, SV_OP_TREE_ATTN_BWD = 3 } sv_op;
 
 /* Human-readable name of a status code (static storage). */
 const char* sv_status_string(sv_status s);
@@ -68,6 +68,7 @@ int sv_version(void);
 /*
  * Bytes of device workspace a call needs (0 if none).  Arguments that do not apply to `op` are ignored:
  *   SV_OP_TREE_ATTN: B, T, Hq, Hkv, D, kv_cap      SV_OP_ACCEPT: B (= rows/T), T, V      SV_OP_LOSS: B (= N), T, V
+ *   SV_OP_TREE_ATTN_BWD: B, T, Hq
  * The result is an upper bound that does not depend on device data, so it can be computed once.
  */
 size_t sv_workspace_size(sv_op op, int B, int T, int Hq, int Hkv, int D, int kv_cap, int V);
@@ -179,6 +180,34 @@ sv_status sv_accept_noalloc(int B, int T, int V, sv_dtype logit_dt, const void* 
 sv_status sv_loss(int N, int T, int V, const void* draft_logits, const int32_t* tokens,
                   const int32_t* parent, const int32_t* labels, float* row_loss, float* sums, void* grad,
                   int32_t* status, void* workspace, size_t ws_bytes, sv_stream_t stream);
+
+/*
+ * sv_tree_attn_bwd -- gradient of sv_tree_attn for training the draft on its trees.
+ *
+ * The draft is trained on every accepted and rejected branch of its logged trees in one batched forward
+ * and backward pass ("Aurora" post, section 2), so the tree attention of that pass needs its gradient under
+ * the same ancestor mask.  Given the forward's inputs, its output `out` and log-sum-exp `lse` (as written by
+ * sv_tree_attn) and the upstream gradient dout = d loss / d out, with p_j = exp(s_j - lse),
+ * s_j = sm_scale <q, k_j> over the allowed set of sv_tree_attn and delta = <dout, out> per query row:
+ *     dq  = sm_scale * sum_j p_j (<dout, v_j> - delta) k_j
+ *     dk_j = sm_scale * sum over query rows that see j of p_j (<dout, v_j> - delta) q
+ *     dv_j = sum over query rows that see j of p_j dout
+ *   q, out, dout  [B, T, Hq, D] in q_dt (SV_F32 or SV_BF16); k_cache, v_cache [B, Hkv, kv_cap, D] in kv_dt
+ *                 (SV_F32 or SV_BF16); kv_len, parent, sm_scale as for sv_tree_attn
+ *   lse           float [B, T, Hq] from the forward
+ *   dq            float [B, T, Hq, D]
+ *   dk, dv        float [B, Hkv, kv_cap, D]: positions [0, kv_len[b] + T) are written (a position no query row
+ *                 sees gets 0); positions from kv_len[b] + T on are not touched
+ *   status        int32 [B] or NULL; a failed request gets zero dq and untouched dk / dv
+ *   workspace: at least sv_workspace_size(SV_OP_TREE_ATTN_BWD, B, T, Hq, ...) bytes (delta per query row)
+ * Shapes: 1 <= T <= 64, Hq % Hkv == 0, D in {32, 64, 128}, (Hq / Hkv) * D <= 2048.  CUDA-core arithmetic in
+ * fp32; results are deterministic (fixed reduction order, no atomics).
+ */
+sv_status sv_tree_attn_bwd(int B, int T, int Hq, int Hkv, int D, int kv_cap, sv_dtype q_dt, sv_dtype kv_dt,
+                           const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_len,
+                           const int32_t* parent, float sm_scale, const void* out, const float* lse,
+                           const void* dout, float* dq, float* dk, float* dv, int32_t* status, void* workspace,
+                           size_t ws_bytes, sv_stream_t stream);
 
 /*
  * sv_kv_compact -- make the accepted path's K/V contiguous after verification.

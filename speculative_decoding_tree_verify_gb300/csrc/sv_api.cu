@@ -40,6 +40,7 @@ size_t sv_workspace_size(sv_op op, int B, int T, int Hq, int Hkv, int D, int kv_
     case SV_OP_TREE_ATTN: return attn_workspace_size(B, T, Hq, Hkv, D, kv_cap);
     case SV_OP_ACCEPT: return accept_workspace_size(B, T, V);
     case SV_OP_LOSS: return loss_workspace_size(B, T, V);
+    case SV_OP_TREE_ATTN_BWD: return attn_bwd_workspace_size(B, T, Hq);
     }
     return 0;
 }
@@ -140,6 +141,31 @@ sv_status sv_loss(int N, int T, int V, const void* draft_logits, const int32_t* 
     if (!workspace || ws_bytes < need || !aligned(workspace, 256)) return SV_ERR_WORKSPACE;
     LossArgs a{N, T, V, draft_logits, tokens, parent, labels, row_loss, sums, grad, status, workspace};
     return from_cuda(launch_loss(a, (cudaStream_t)stream));
+}
+
+sv_status sv_tree_attn_bwd(int B, int T, int Hq, int Hkv, int D, int kv_cap, sv_dtype q_dt, sv_dtype kv_dt,
+                           const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_len,
+                           const int32_t* parent, float sm_scale, const void* out, const float* lse,
+                           const void* dout, float* dq, float* dk, float* dv, int32_t* status, void* workspace,
+                           size_t ws_bytes, sv_stream_t stream) {
+    if (T > SV_MAX_T) return SV_ERR_TREE_TOO_LARGE;
+    if (B < 0 || B > 65535 || T < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || kv_cap < T) return SV_ERR_INVALID_ARG;
+    if (!(sm_scale >= 0.f) || isinf(sm_scale)) return SV_ERR_INVALID_ARG;
+    if ((q_dt != SV_F32 && q_dt != SV_BF16) || (kv_dt != SV_F32 && kv_dt != SV_BF16)) return SV_ERR_UNSUPPORTED;
+    if ((D != 32 && D != 64 && D != 128) || (size_t)(Hq / Hkv) * D > 2048) return SV_ERR_UNSUPPORTED;
+    if (Hkv > 65535 || (kv_cap + 15) / 16 > 0x7fffffff) return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!q || !k_cache || !v_cache || !kv_len || !parent || !out || !lse || !dout || !dq || !dk || !dv)
+        return SV_ERR_INVALID_ARG;
+    if (!aligned(q, 4) || !aligned(k_cache, 4) || !aligned(v_cache, 4) || !aligned(out, 4) || !aligned(dout, 4) ||
+        !aligned(lse, 4) || !aligned(dq, 4) || !aligned(dk, 4) || !aligned(dv, 4) || !aligned(kv_len, 4) ||
+        !aligned(parent, 4) || !aligned(status, 4))
+        return SV_ERR_UNSUPPORTED;
+    const size_t need = attn_bwd_workspace_size(B, T, Hq);
+    if (!workspace || ws_bytes < need || !aligned(workspace, 256)) return SV_ERR_WORKSPACE;
+    AttnBwdArgs a{B, T, Hq, Hkv, D, kv_cap, q_dt, kv_dt, q, k_cache, v_cache, kv_len, parent, sm_scale, out, lse,
+                  dout, dq, dk, dv, (float*)workspace, status};
+    return from_cuda(launch_attn_bwd(a, (cudaStream_t)stream));
 }
 
 sv_status sv_kv_compact(int B, int T, int Hkv, int D, int kv_cap, sv_dtype kv_dt, void* k_cache, void* v_cache,

@@ -122,6 +122,28 @@ struct LossArgs {
 size_t loss_workspace_size(int N, int T, int V);
 cudaError_t launch_loss(const LossArgs& a, cudaStream_t s);
 
+struct AttnBwdArgs {
+    int B, T, Hq, Hkv, D, kv_cap;
+    sv_dtype q_dt, kv_dt;
+    const void* q;
+    const void* k;
+    const void* v;
+    const int32_t* kv_len;
+    const int32_t* parent;
+    float sm_scale;
+    const void* out;
+    const float* lse;
+    const void* dout;
+    float* dq;
+    float* dk;
+    float* dv;
+    float* delta;   // workspace [B, T, Hq]
+    int32_t* status;
+};
+
+size_t attn_bwd_workspace_size(int B, int T, int Hq);
+cudaError_t launch_attn_bwd(const AttnBwdArgs& a, cudaStream_t s);
+
 struct CompactArgs {
     int B, T, Hkv, D, kv_cap;
     sv_dtype kv_dt;

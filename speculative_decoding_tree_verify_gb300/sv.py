@@ -17,7 +17,7 @@ LIB_PATH = Path(__file__).resolve().parent / "_build" / "libsv.so"
 OK, ERR_INVALID_ARG, ERR_BAD_TREE, ERR_TREE_TOO_LARGE, ERR_UNSUPPORTED, ERR_NONFINITE, ERR_TIMEOUT, ERR_CUDA, \
     ERR_WORKSPACE = range(9)
 F32, BF16, E4M3 = 0, 1, 2
-OP_TREE_ATTN, OP_ACCEPT, OP_LOSS = 0, 1, 2
+OP_TREE_ATTN, OP_ACCEPT, OP_LOSS, OP_TREE_ATTN_BWD = 0, 1, 2, 3
 
 _lib = None
 
@@ -49,6 +49,8 @@ def lib() -> C.CDLL:
         L.sv_loss.restype = i
         L.sv_accept_noalloc.argtypes = [i, i, i, i, P, P, P, P, f, P, P, P, P, P, P, P, P]
         L.sv_accept_noalloc.restype = i
+        L.sv_tree_attn_bwd.argtypes = [i, i, i, i, i, i, i, i, P, P, P, P, P, f, P, P, P, P, P, P, P, P, z, P]
+        L.sv_tree_attn_bwd.restype = i
         L.sv_kv_compact.argtypes = [i, i, i, i, i, i, P, P, P, P, P, P, P, P, P]
         L.sv_kv_compact.restype = i
         L.sv_tree_expand.argtypes = [i, i, i, i, i, i, P, P, P, P, P, P, P, P, P]
@@ -169,3 +171,16 @@ def tree_expand(logits, front_score, k, n_keep, topk_token, topk_logprob, child_
                                 _ptr(front_score), _ptr(topk_token), _ptr(topk_logprob), _ptr(child_parent),
                                 _ptr(child_token), _ptr(child_score), _ptr(status), _stream(stream))
     _check(code, "sv_tree_expand")
+
+
+def tree_attn_bwd(q, k_cache, v_cache, kv_len, parent, out, lse, dout, dq, dk, dv, *, sm_scale=0.0, status=None,
+                  workspace=None, stream=None):
+    """sv_tree_attn_bwd: forward inputs plus out / lse / dout [B,T,Hq,D]; dq like q (fp32); dk, dv like the caches (fp32)."""
+    B, T, Hq, D = q.shape
+    Hkv, kv_cap = k_cache.shape[1], k_cache.shape[2]
+    ws = _ws(OP_TREE_ATTN_BWD, workspace, B, T, Hq, Hkv, D, kv_cap, 0)
+    code = lib().sv_tree_attn_bwd(B, T, Hq, Hkv, D, kv_cap, dtype_code(q), dtype_code(k_cache), _ptr(q), _ptr(k_cache),
+                                  _ptr(v_cache), _ptr(kv_len), _ptr(parent), float(sm_scale), _ptr(out), _ptr(lse),
+                                  _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(status), _ptr(ws),
+                                  ws.numel() * ws.element_size(), _stream(stream))
+    _check(code, "sv_tree_attn_bwd")

@@ -122,6 +122,33 @@ def test_loss_host_validation(L):
     assert loss(L, ws=None) == sv.ERR_WORKSPACE
 
 
+def attn_bwd(L, **kw):
+    a = dict(B=2, T=4, Hq=4, Hkv=2, D=64, kv_cap=64, q_dt=sv.BF16, kv_dt=sv.BF16, q=FAKE, k=FAKE, v=FAKE,
+             kv_len=FAKE, parent=FAKE, scale=0.0, out=FAKE, lse=FAKE, dout=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, st=None,
+             ws=FAKE, ws_bytes=1 << 20)
+    a.update(kw)
+    return L.sv_tree_attn_bwd(a["B"], a["T"], a["Hq"], a["Hkv"], a["D"], a["kv_cap"], a["q_dt"], a["kv_dt"], a["q"],
+                              a["k"], a["v"], a["kv_len"], a["parent"], a["scale"], a["out"], a["lse"], a["dout"],
+                              a["dq"], a["dk"], a["dv"], a["st"], a["ws"], a["ws_bytes"], None)
+
+
+def test_tree_attn_bwd_host_validation(L):
+    assert attn_bwd(L, T=65) == sv.ERR_TREE_TOO_LARGE
+    assert attn_bwd(L, Hq=3) == sv.ERR_INVALID_ARG
+    assert attn_bwd(L, kv_cap=2) == sv.ERR_INVALID_ARG
+    assert attn_bwd(L, scale=-1.0) == sv.ERR_INVALID_ARG
+    assert attn_bwd(L, kv_dt=sv.E4M3) == sv.ERR_UNSUPPORTED       # the backward takes bf16 / fp32 caches
+    assert attn_bwd(L, D=96) == sv.ERR_UNSUPPORTED
+    assert attn_bwd(L, Hq=64, Hkv=2, D=128) == sv.ERR_UNSUPPORTED  # G * D above 2048
+    assert attn_bwd(L, lse=None) == sv.ERR_INVALID_ARG
+    assert attn_bwd(L, dv=None) == sv.ERR_INVALID_ARG
+    assert attn_bwd(L, dq=ODD) == sv.ERR_UNSUPPORTED
+    assert attn_bwd(L, ws=None) == sv.ERR_WORKSPACE
+    assert attn_bwd(L, ws_bytes=8) == sv.ERR_WORKSPACE
+    assert attn_bwd(L, B=0) == sv.OK
+    assert sv.workspace_size(sv.OP_TREE_ATTN_BWD, 8, 60, 32) >= 8 * 60 * 32 * 4
+
+
 def compact(L, **kw):
     a = dict(B=2, T=4, Hkv=2, D=64, kv_cap=64, dt=sv.BF16, k=FAKE, v=FAKE, kv_len=FAKE, par=FAKE, al=FAKE, path=FAKE,
              nl=C.c_void_p(0x200000), st=None)
