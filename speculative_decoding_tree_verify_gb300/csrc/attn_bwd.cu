@@ -44,9 +44,9 @@ __global__ void __launch_bounds__(kThreads) attn_bwd_dq_kernel(AttnBwdArgs a, fl
     float* qs = smem;                       // [G][D]
     float* gs = qs + G * D;                 // [G][D]  dO
     float* dqs = gs + G * D;                // [G][D]  accumulators
-    float* ks = dqs + G * D;                // [kTileQ][D+1]
-    float* vs = ks + kTileQ * (D + 1);      // [kTileQ][D+1]
-    float* lses = vs + kTileQ * (D + 1);    // [G]  lse * log2(e)
+    float* ks = dqs + G * D;                // [kTileQ][D+4]: rows 16-byte aligned for float4 reads
+    float* vs = ks + kTileQ * (D + 4);      // [kTileQ][D+4]
+    float* lses = vs + kTileQ * (D + 4);    // [G]  lse * log2(e)
     float* dls = lses + G;                  // [G]  delta
     __shared__ int32_t s_par[SV_MAX_T];
     __shared__ int32_t s_anc[SV_MAX_T];
@@ -94,17 +94,32 @@ __global__ void __launch_bounds__(kThreads) attn_bwd_dq_kernel(AttnBwdArgs a, fl
     const int npos = L + s_nanc;
     const float sl2 = scale * kLog2e;
     for (int start = 0; start < npos; start += kTileQ) {
-        for (int i = tid; i < kTileQ * D; i += kThreads) {
-            const int r = i / D, d = i - r * D;
-            const int j = start + r;
-            float kx = 0.f, vx = 0.f;
-            if (j < npos) {
-                const size_t pos = (size_t)(j < L ? j : s_anc[j - L]);
-                kx = KE::get(kp, pos * D + d);
-                vx = KE::get(vp, pos * D + d);
+        // all loads of a batch are issued before any is used, so a tile costs one memory round trip
+        constexpr int kBatch = 16;
+        for (int base = 0; base < kTileQ * D; base += kThreads * kBatch) {
+            float kx[kBatch], vx[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int i = base + u * kThreads + tid;
+                const int r = i / D, d = i - r * D;
+                const int j = start + r;
+                kx[u] = 0.f;
+                vx[u] = 0.f;
+                if (i < kTileQ * D && j < npos) {
+                    const size_t pos = (size_t)(j < L ? j : s_anc[j - L]);
+                    kx[u] = KE::get(kp, pos * D + d);
+                    vx[u] = KE::get(vp, pos * D + d);
+                }
             }
-            ks[r * (D + 1) + d] = kx;
-            vs[r * (D + 1) + d] = vx;
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int i = base + u * kThreads + tid;
+                if (i < kTileQ * D) {
+                    const int r = i / D, d = i - r * D;
+                    ks[r * (D + 4) + d] = kx[u];
+                    vs[r * (D + 4) + d] = vx[u];
+                }
+            }
         }
         __syncthreads();
         for (int g = warp; g < G; g += kThreads / 32) {
@@ -112,17 +127,19 @@ __global__ void __launch_bounds__(kThreads) attn_bwd_dq_kernel(AttnBwdArgs a, fl
             if (start + lane < npos) {
                 const float* qr = qs + g * D;
                 const float* gr = gs + g * D;
-                const float* kr = ks + lane * (D + 1);
-                const float* vr = vs + lane * (D + 1);
+                const float* kr = ks + lane * (D + 4);
+                const float* vr = vs + lane * (D + 4);
                 float s0 = 0.f, s1 = 0.f, p0 = 0.f, p1 = 0.f;
-                int d = 0;
-                for (; d + 1 < D; d += 2) {
-                    s0 = fmaf(qr[d], kr[d], s0);
-                    s1 = fmaf(qr[d + 1], kr[d + 1], s1);
-                    p0 = fmaf(gr[d], vr[d], p0);
-                    p1 = fmaf(gr[d + 1], vr[d + 1], p1);
+                for (int d = 0; d < D; d += 4) {   // D is a multiple of 32
+                    const float4 qa = *reinterpret_cast<const float4*>(qr + d);
+                    const float4 ka = *reinterpret_cast<const float4*>(kr + d);
+                    const float4 ga = *reinterpret_cast<const float4*>(gr + d);
+                    const float4 va = *reinterpret_cast<const float4*>(vr + d);
+                    s0 = fmaf(qa.x, ka.x, s0); s1 = fmaf(qa.y, ka.y, s1);
+                    s0 = fmaf(qa.z, ka.z, s0); s1 = fmaf(qa.w, ka.w, s1);
+                    p0 = fmaf(ga.x, va.x, p0); p1 = fmaf(ga.y, va.y, p1);
+                    p0 = fmaf(ga.z, va.z, p0); p1 = fmaf(ga.w, va.w, p1);
                 }
-                if (d < D) { s0 = fmaf(qr[d], kr[d], s0); p0 = fmaf(gr[d], vr[d], p0); }
                 const float p = exp2f(fmaf(s0 + s1, sl2, -lses[g]));
                 ds = p * ((p0 + p1) - dls[g]);
             }
@@ -130,8 +147,8 @@ __global__ void __launch_bounds__(kThreads) attn_bwd_dq_kernel(AttnBwdArgs a, fl
                 float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
                 for (int j = 0; j < kTileQ; j += 2) {
-                    acc0 = fmaf(__shfl_sync(0xffffffffu, ds, j), ks[j * (D + 1) + d], acc0);
-                    acc1 = fmaf(__shfl_sync(0xffffffffu, ds, j + 1), ks[(j + 1) * (D + 1) + d], acc1);
+                    acc0 = fmaf(__shfl_sync(0xffffffffu, ds, j), ks[j * (D + 4) + d], acc0);
+                    acc1 = fmaf(__shfl_sync(0xffffffffu, ds, j + 1), ks[(j + 1) * (D + 4) + d], acc1);
                 }
                 dqs[g * D + d] += acc0 + acc1;
             }
@@ -203,17 +220,30 @@ __global__ void __launch_bounds__(kThreads) attn_bwd_dkv_kernel(AttnBwdArgs a, f
     const typename QE::T* q = (const typename QE::T*)a.q;
     const typename QE::T* go = (const typename QE::T*)a.dout;
     const float sl2 = scale * kLog2e;
-    for (int rr = warp; rr < T * G; rr += NW) {
+    // each warp walks its rows with the next row's q, dO, lse and delta already in flight
+    const int TG = T * G;
+    float qn[DL], gn[DL], lsen = 0.f, dln = 0.f;
+    auto fetch = [&](int rr) {
         const int i = rr / G, g = rr - i * G;
-        const unsigned long long anc = s_anc[i];
-        if (!has_prefix && !(anc & tile_tree)) continue;   // the row sees none of these positions
         const size_t row = ((size_t)b * T + i) * a.Hq + (size_t)hk * G + g;
-        float qv[DL], gv[DL];
 #pragma unroll
         for (int m = 0; m < DL; ++m) {
-            qv[m] = QE::get(q, row * D + lane + 32 * m);
-            gv[m] = QE::get(go, row * D + lane + 32 * m);
+            qn[m] = QE::get(q, row * D + lane + 32 * m);
+            gn[m] = QE::get(go, row * D + lane + 32 * m);
         }
+        lsen = a.lse[row];
+        dln = a.delta[row];
+    };
+    if (warp < TG) fetch(warp);
+    for (int rr = warp; rr < TG; rr += NW) {
+        const int i = rr / G;
+        float qv[DL], gv[DL];
+#pragma unroll
+        for (int m = 0; m < DL; ++m) { qv[m] = qn[m]; gv[m] = gn[m]; }
+        const float lse_r = lsen, delta_r = dln;
+        if (rr + NW < TG) fetch(rr + NW);
+        const unsigned long long anc = s_anc[i];
+        if (!has_prefix && !(anc & tile_tree)) continue;   // the row sees none of these positions
         float sp[kTileKV], dpp[kTileKV];
 #pragma unroll
         for (int j = 0; j < kTileKV; ++j) {
@@ -230,9 +260,8 @@ __global__ void __launch_bounds__(kThreads) attn_bwd_dkv_kernel(AttnBwdArgs a, f
         const float dp_tot = reduce16(dpp, lane);
         const int jl = lane >> 1, jabs = j0 + jl;
         const bool allowed = jl < nj && (jabs < L || ((anc >> (jabs - L)) & 1ull));
-        const float lse2 = a.lse[row] * kLog2e;
-        const float p = allowed ? exp2f(fmaf(s_tot, sl2, -lse2)) : 0.f;
-        const float ds = p * (dp_tot - a.delta[row]);
+        const float p = allowed ? exp2f(fmaf(s_tot, sl2, -lse_r * kLog2e)) : 0.f;
+        const float ds = p * (dp_tot - delta_r);
 #pragma unroll
         for (int j = 0; j < kTileKV; ++j) {
             const float pj = __shfl_sync(0xffffffffu, p, 2 * j);
@@ -271,7 +300,7 @@ __global__ void __launch_bounds__(kThreads) attn_bwd_dkv_kernel(AttnBwdArgs a, f
 template <int QDT, int KVDT>
 cudaError_t launch_typed(const AttnBwdArgs& a, cudaStream_t s) {
     const int G = a.Hq / a.Hkv;
-    const size_t smem = sizeof(float) * ((size_t)3 * G * a.D + (size_t)2 * kTileQ * (a.D + 1) + 2 * G);
+    const size_t smem = sizeof(float) * ((size_t)3 * G * a.D + (size_t)2 * kTileQ * (a.D + 4) + 2 * G);
     auto k1 = attn_bwd_dq_kernel<QDT, KVDT>;
     cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
