@@ -104,6 +104,28 @@ sv_status sv_tree_attn(int B, int T, int Hq, int Hkv, int D, int kv_cap, sv_dtyp
                        sv_stream_t stream);
 
 /*
+ * sv_tree_attn_paged -- sv_tree_attn over a paged KV cache.
+ *
+ * Serving systems keep the KV cache in fixed-size pages shared by all requests and give each request a
+ * page table.  The attention is exactly sv_tree_attn's ("Aurora" post, section 2) over each request's
+ * logical cache, whose position j (0 <= j < max_pages * page_size) lives at
+ *     pool[page_table[b, j / page_size], hk, j % page_size, :]
+ * with the tree's own K/V at logical positions kv_len[b] .. kv_len[b] + T - 1, as in sv_tree_attn.
+ *   k_pool, v_pool  [num_pages, Hkv, page_size, D] in kv_dt (SV_F32, SV_BF16, SV_E4M3 + per-head scales)
+ *   page_table      int32 [B, max_pages]; entries past the pages a request reads are ignored
+ *   page_size       a power of two
+ *   q, out, lse, kv_len, parent, sm_scale, status: as for sv_tree_attn, with kv_cap = max_pages * page_size
+ * A request whose kv_len + T exceeds max_pages * page_size, or that reads a page id outside
+ * [0, num_pages), gets status SV_ERR_INVALID_ARG and zero outputs.  Runs on the CUDA-core attention kernel
+ * (fp32 arithmetic, any D up to 256); no workspace.
+ */
+sv_status sv_tree_attn_paged(int B, int T, int Hq, int Hkv, int D, int page_size, int max_pages, int num_pages,
+                             sv_dtype q_dt, sv_dtype kv_dt, const void* q, const void* k_pool, const void* v_pool,
+                             const float* k_scale, const float* v_scale, const int32_t* page_table,
+                             const int32_t* kv_len, const int32_t* parent, float sm_scale, void* out, float* lse,
+                             int32_t* status, sv_stream_t stream);
+
+/*
  * sv_accept -- verify one batch of draft trees against the target's per-node logits.
  *
  * Row i of request b (target_logits[b, i, :]) is the target's next-token logits after node i.  The walk

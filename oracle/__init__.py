@@ -137,6 +137,39 @@ def tree_attn_w(w, rows=None, sm_scale=0.0):
                      k_scale=w.k_scale, v_scale=w.v_scale, sm_scale=sm_scale, rows=rows)
 
 
+def tree_attn_paged(q, k_pool, v_pool, page_table, kv_len, parent, *, Hq, Hkv, q_dt, kv_dt, k_scale=None,
+                    v_scale=None, sm_scale=0.0):
+    """Tree attention over paged caches: each request's logical cache is read through its page table (pool
+    page page_table[b, j // P] holds positions j), then the plain definition above runs on it.  A request
+    whose kv_len + T exceeds the table's capacity or that names a page outside the pool gets status 1."""
+    num_pages, _, P, D = k_pool.shape
+    B, max_pages = page_table.shape
+    T = parent.shape[1]
+    cap = max_pages * P
+    junk = np.zeros((), dtype=k_pool.dtype)
+    k = np.full((B, Hkv, cap, D), junk, dtype=k_pool.dtype)
+    v = np.full((B, Hkv, cap, D), junk, dtype=v_pool.dtype)
+    bad = np.zeros(B, bool)
+    for b in range(B):
+        n = int(kv_len[b]) + T
+        if n > cap or int(kv_len[b]) < 0:
+            bad[b] = True
+            continue
+        for pg in range(-(-n // P)):
+            src = int(page_table[b, pg])
+            if not 0 <= src < num_pages:
+                bad[b] = True
+                break
+            k[b, :, pg * P:(pg + 1) * P] = k_pool[src]
+            v[b, :, pg * P:(pg + 1) * P] = v_pool[src]
+    out, lse, status, rc = tree_attn(q, k, v, kv_len, parent, Hq=Hq, Hkv=Hkv, q_dt=q_dt, kv_dt=kv_dt,
+                                     k_scale=k_scale, v_scale=v_scale, sm_scale=sm_scale)
+    status = np.where(bad & (status == 0), 1, status).astype(np.int32)
+    out[bad] = 0.0
+    lse[bad] = 0.0
+    return out, lse, status, rc
+
+
 def tree_attn_bwd(q, k, v, kv_len, parent, dout, *, Hq, Hkv, q_dt, kv_dt, sm_scale=0.0):
     """float64 backward of the tree-masked attention for the upstream gradient dout (q's layout and dtype).
     Returns (dq [B,T,Hq,D], dk [B,Hkv,kv_cap,D], dv [B,Hkv,kv_cap,D], status [B], rc)."""

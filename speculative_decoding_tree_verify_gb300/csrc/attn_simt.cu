@@ -38,6 +38,12 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(AttnArgs a, float s
     const int L = a.kv_len[b];
     int st = block_tree_check(s_par, T);
     if (st == SV_OK && (L < 0 || L + T > a.kv_cap)) st = SV_ERR_INVALID_ARG;
+    const int32_t* pt = a.page_table ? a.page_table + (size_t)b * a.max_pages : nullptr;
+    if (pt && st == SV_OK) {   // every page the request reads must name a page of the pool
+        int bad = 0;
+        for (int i = tid; i < ((L + T - 1) >> a.page_shift) + 1; i += kThreads) bad |= pt[i] < 0 || pt[i] >= a.num_pages;
+        if (__syncthreads_or(bad)) st = SV_ERR_INVALID_ARG;
+    }
 
     const size_t out_row0 = ((size_t)b * T + t) * a.Hq + (size_t)hk * G;
     if (st != SV_OK) {
@@ -66,8 +72,15 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(AttnArgs a, float s
 
     const float ksc = (KVDT == SV_E4M3) ? a.k_scale[hk] : 1.f;
     const float vsc = (KVDT == SV_E4M3) ? a.v_scale[hk] : 1.f;
-    const typename KE::T* kp = (const typename KE::T*)a.k + ((size_t)b * a.Hkv + hk) * (size_t)a.kv_cap * D;
-    const typename KE::T* vp = (const typename KE::T*)a.v + ((size_t)b * a.Hkv + hk) * (size_t)a.kv_cap * D;
+    // contiguous caches: the (request, kv head) block; paged caches: the pool, rows found through pt
+    const size_t blk = pt ? 0 : ((size_t)b * a.Hkv + hk) * (size_t)a.kv_cap * D;
+    const typename KE::T* kp = (const typename KE::T*)a.k + blk;
+    const typename KE::T* vp = (const typename KE::T*)a.v + blk;
+    const int pmask = (1 << a.page_shift) - 1;
+    auto cache_row = [&](int pos) -> size_t {
+        if (!pt) return (size_t)pos;
+        return ((size_t)__ldg(pt + (pos >> a.page_shift)) * a.Hkv + hk) * (size_t)(pmask + 1) + (pos & pmask);
+    };
     const int npos = L + s_nanc;
 
     for (int start = 0; start < npos; start += kTile) {
@@ -83,9 +96,9 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(AttnArgs a, float s
                 kv[u] = 0.f;
                 vv[u] = 0.f;
                 if (i < kTile * D && j < npos) {
-                    const size_t pos = (size_t)(j < L ? j : s_anc[j - L]);
-                    kv[u] = KE::get(kp, pos * D + d);
-                    vv[u] = KE::get(vp, pos * D + d);
+                    const size_t row = cache_row(j < L ? j : s_anc[j - L]);
+                    kv[u] = KE::get(kp, row * D + d);
+                    vv[u] = KE::get(vp, row * D + d);
                 }
             }
 #pragma unroll

@@ -72,6 +72,37 @@ sv_status sv_tree_attn(int B, int T, int Hq, int Hkv, int D, int kv_cap, sv_dtyp
     return from_cuda(tc ? launch_attn_tc(a, s) : launch_attn_simt(a, s));
 }
 
+sv_status sv_tree_attn_paged(int B, int T, int Hq, int Hkv, int D, int page_size, int max_pages, int num_pages,
+                             sv_dtype q_dt, sv_dtype kv_dt, const void* q, const void* k_pool, const void* v_pool,
+                             const float* k_scale, const float* v_scale, const int32_t* page_table,
+                             const int32_t* kv_len, const int32_t* parent, float sm_scale, void* out, float* lse,
+                             int32_t* status, sv_stream_t stream) {
+    if (T > SV_MAX_T) return SV_ERR_TREE_TOO_LARGE;
+    if (B < 0 || B > 65535 || T < 1 || Hq < 1 || Hkv < 1 || Hkv > 65535 || Hq % Hkv || D < 1) return SV_ERR_INVALID_ARG;
+    if (page_size < 1 || (page_size & (page_size - 1)) || max_pages < 1 || num_pages < 1) return SV_ERR_INVALID_ARG;
+    if ((long long)page_size * max_pages > 0x7fffffffLL || (long long)page_size * max_pages < T) return SV_ERR_INVALID_ARG;
+    if (!(sm_scale >= 0.f) || isinf(sm_scale)) return SV_ERR_INVALID_ARG;
+    if ((q_dt != SV_F32 && q_dt != SV_BF16) || (kv_dt != SV_F32 && kv_dt != SV_BF16 && kv_dt != SV_E4M3))
+        return SV_ERR_UNSUPPORTED;
+    if (D > 256 || (size_t)(Hq / Hkv) * D > 4096) return SV_ERR_UNSUPPORTED;
+    if (B == 0) return SV_OK;
+    if (!q || !k_pool || !v_pool || !page_table || !kv_len || !parent || !out) return SV_ERR_INVALID_ARG;
+    if (kv_dt == SV_E4M3 && (!k_scale || !v_scale)) return SV_ERR_INVALID_ARG;
+    if (!aligned(q, 4) || !aligned(k_pool, 4) || !aligned(v_pool, 4) || !aligned(out, 4) || !aligned(page_table, 4) ||
+        !aligned(kv_len, 4) || !aligned(parent, 4) || !aligned(lse, 4) || !aligned(status, 4) ||
+        !aligned(k_scale, 4) || !aligned(v_scale, 4))
+        return SV_ERR_UNSUPPORTED;
+    int shift = 0;
+    while ((1 << shift) < page_size) ++shift;
+    AttnArgs a{B, T, Hq, Hkv, D, page_size * max_pages, q_dt, kv_dt, q, k_pool, v_pool, k_scale, v_scale, kv_len,
+               parent, sm_scale, out, lse, status, nullptr, 0};
+    a.page_table = page_table;
+    a.page_shift = shift;
+    a.max_pages = max_pages;
+    a.num_pages = num_pages;
+    return from_cuda(launch_attn_simt(a, (cudaStream_t)stream));
+}
+
 sv_status sv_accept(int B, int T, int V, sv_dtype logit_dt, const void* target_logits,
                     const void* draft_logits, const int32_t* tokens, const int32_t* parent, float temperature,
                     const uint32_t* uniforms, int32_t* accept_len, int32_t* path, int32_t* out_tokens,

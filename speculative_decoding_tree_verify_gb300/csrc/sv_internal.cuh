@@ -75,6 +75,12 @@ struct AttnArgs {
     int32_t* status;
     void* ws;
     size_t ws_bytes;
+    // paged caches (CUDA-core path only): k / v are pools [num_pages, Hkv, page_size, D]; logical position j
+    // of request b lives in page page_table[b * max_pages + j / page_size] at offset j % page_size
+    const int32_t* page_table = nullptr;
+    int page_shift = 0;   // log2(page_size)
+    int max_pages = 0;
+    int num_pages = 0;
 };
 
 size_t attn_workspace_size(int B, int T, int Hq, int Hkv, int D, int kv_cap);

@@ -49,6 +49,8 @@ def lib() -> C.CDLL:
         L.sv_loss.restype = i
         L.sv_accept_noalloc.argtypes = [i, i, i, i, P, P, P, P, f, P, P, P, P, P, P, P, P]
         L.sv_accept_noalloc.restype = i
+        L.sv_tree_attn_paged.argtypes = [i, i, i, i, i, i, i, i, i, i, P, P, P, P, P, P, P, P, f, P, P, P, P]
+        L.sv_tree_attn_paged.restype = i
         L.sv_tree_attn_bwd.argtypes = [i, i, i, i, i, i, i, i, P, P, P, P, P, f, P, P, P, P, P, P, P, P, z, P]
         L.sv_tree_attn_bwd.restype = i
         L.sv_kv_compact.argtypes = [i, i, i, i, i, i, P, P, P, P, P, P, P, P, P]
@@ -116,6 +118,19 @@ def tree_attn(q, k_cache, v_cache, kv_len, parent, out, *, k_scale=None, v_scale
                               float(sm_scale), _ptr(out), _ptr(lse), _ptr(status), _ptr(ws),
                               0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
     _check(code, "sv_tree_attn")
+
+
+def tree_attn_paged(q, k_pool, v_pool, page_table, kv_len, parent, out, *, k_scale=None, v_scale=None, sm_scale=0.0,
+                    lse=None, status=None, stream=None):
+    """sv_tree_attn_paged: q [B,T,Hq,D]; pools [num_pages,Hkv,page_size,D]; page_table [B,max_pages]; out like q."""
+    B, T, Hq, D = q.shape
+    num_pages, Hkv, page_size = k_pool.shape[0], k_pool.shape[1], k_pool.shape[2]
+    max_pages = page_table.shape[1]
+    code = lib().sv_tree_attn_paged(B, T, Hq, Hkv, D, page_size, max_pages, num_pages, dtype_code(q),
+                                    dtype_code(k_pool), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
+                                    _ptr(v_scale), _ptr(page_table), _ptr(kv_len), _ptr(parent), float(sm_scale),
+                                    _ptr(out), _ptr(lse), _ptr(status), _stream(stream))
+    _check(code, "sv_tree_attn_paged")
 
 
 def accept(target_logits, tokens, parent, accept_len, path, out_tokens, bonus, *, draft_logits=None,

@@ -327,6 +327,37 @@ def make_loss(seed: int, *, N: int, T: int, V: int, tree=(4, 3, 2, 1, 1), sigma:
 
 
 # ----------------------------------------------------------------------------------------------------
+# paged KV caches
+# ----------------------------------------------------------------------------------------------------
+def to_pages(seed: int, cache: np.ndarray, kv_len: np.ndarray, T: int, page_size: int, extra_pages: int = 3,
+             junk=None):
+    """Scatter a contiguous cache [B, Hkv, kv_cap, D] into a page pool [num_pages, Hkv, page_size, D] with a
+    random page table [B, max_pages] (max_pages = ceil(kv_cap / page_size)).  Every page a request uses
+    (those covering positions < kv_len + T) gets a distinct pool page in random order; unused table entries
+    are -1; the pool holds `extra_pages` pages nobody uses, filled with `junk` (or zeros).  Data layout only."""
+    (s_perm,) = rng_streams(seed, 1)
+    B, Hkv, cap, D = cache.shape
+    max_pages = -(-cap // page_size)
+    used = [-(-(int(kv_len[b]) + T) // page_size) for b in range(B)]
+    num_pages = sum(used) + extra_pages
+    perm = s_perm.permutation(num_pages)
+    pool = np.zeros((num_pages, Hkv, page_size, D), dtype=cache.dtype)
+    if junk is not None:
+        pool[...] = junk
+    table = np.full((B, max_pages), -1, np.int32)
+    k = 0
+    for b in range(B):
+        for pg in range(used[b]):
+            dst = int(perm[k])
+            k += 1
+            table[b, pg] = dst
+            lo = pg * page_size
+            n = min(page_size, cap - lo)
+            pool[dst, :, :n] = cache[b, :, lo:lo + n]
+    return pool, table
+
+
+# ----------------------------------------------------------------------------------------------------
 # KV compaction inputs: accepted root paths
 # ----------------------------------------------------------------------------------------------------
 def random_root_paths(seed: int, parent: np.ndarray, stop_p: float = 0.3, full_p: float = 0.2):

@@ -122,6 +122,31 @@ def test_loss_host_validation(L):
     assert loss(L, ws=None) == sv.ERR_WORKSPACE
 
 
+def paged(L, **kw):
+    a = dict(B=2, T=4, Hq=4, Hkv=2, D=64, P=16, maxp=8, nump=20, q_dt=sv.BF16, kv_dt=sv.BF16, q=FAKE, k=FAKE, v=FAKE,
+             ks=None, vs=None, pt=FAKE, kv_len=FAKE, parent=FAKE, scale=0.0, out=FAKE, lse=None, st=None)
+    a.update(kw)
+    return L.sv_tree_attn_paged(a["B"], a["T"], a["Hq"], a["Hkv"], a["D"], a["P"], a["maxp"], a["nump"], a["q_dt"],
+                                a["kv_dt"], a["q"], a["k"], a["v"], a["ks"], a["vs"], a["pt"], a["kv_len"], a["parent"],
+                                a["scale"], a["out"], a["lse"], a["st"], None)
+
+
+def test_tree_attn_paged_host_validation(L):
+    assert paged(L, T=65) == sv.ERR_TREE_TOO_LARGE
+    assert paged(L, P=24) == sv.ERR_INVALID_ARG                # page size not a power of two
+    assert paged(L, P=0) == sv.ERR_INVALID_ARG
+    assert paged(L, maxp=0) == sv.ERR_INVALID_ARG
+    assert paged(L, P=1, maxp=3) == sv.ERR_INVALID_ARG         # capacity below T
+    assert paged(L, nump=0) == sv.ERR_INVALID_ARG
+    assert paged(L, Hq=3) == sv.ERR_INVALID_ARG
+    assert paged(L, q_dt=sv.E4M3) == sv.ERR_UNSUPPORTED
+    assert paged(L, D=512) == sv.ERR_UNSUPPORTED
+    assert paged(L, pt=None) == sv.ERR_INVALID_ARG
+    assert paged(L, kv_dt=sv.E4M3) == sv.ERR_INVALID_ARG       # e4m3 needs its scales
+    assert paged(L, k=ODD) == sv.ERR_UNSUPPORTED
+    assert paged(L, B=0) == sv.OK
+
+
 def attn_bwd(L, **kw):
     a = dict(B=2, T=4, Hq=4, Hkv=2, D=64, kv_cap=64, q_dt=sv.BF16, kv_dt=sv.BF16, q=FAKE, k=FAKE, v=FAKE,
              kv_len=FAKE, parent=FAKE, scale=0.0, out=FAKE, lse=FAKE, dout=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, st=None,
