@@ -640,10 +640,11 @@ int or_tree_expand(int B, int n_front, int V, int k, int n_keep, int logit_dt, c
 static void attn_row_bwd(int T, int Hq, int Hkv, int D, int kv_cap, int q_dt, int kv_dt, const void* q,
                          const void* k, const void* v, const void* dout, int L, const int32_t* par,
                          double scale, int b, int i, int h, double* dq, double* dk, double* dv) {
-    int G = Hq / Hkv, hk = h / G;
+    const int G = Hq / Hkv;
+    const int hk = h / G;                               /* contiguous GQA groups, as in the forward */
     int on[64];
     memset(on, 0, sizeof on);
-    for (int a = i; a >= 0; a = par[a]) on[a] = 1;
+    for (int x = i; x >= 0; x = par[x]) on[x] = 1;   /* the node, its ancestors and the root */
     size_t qoff = (((size_t)b * T + i) * Hq + h) * D;
     size_t kvbase = ((size_t)b * Hkv + hk) * (size_t)kv_cap * D;
     int npos = L + T;
@@ -657,7 +658,7 @@ static void attn_row_bwd(int T, int Hq, int Hkv, int D, int kv_cap, int q_dt, in
         if (!(j < L || on[j - L])) { s[j] = -INFINITY; continue; }
         double acc = 0.0;
         for (int d = 0; d < D; ++d) acc += qv[d] * load_elem(k, kvbase + (size_t)j * D + d, kv_dt);
-        s[j] = scale * acc;
+        s[j] = acc * scale;
         if (s[j] > m) m = s[j];
     }
     double sum = 0.0;
