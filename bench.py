@@ -59,6 +59,28 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+# ------------------------------------------------------------------------------------------ ranks
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest value of x over all ranks (the slowest rank's step time); x itself on one rank."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def nodes_per_second(B: int, T: int, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank verifies its own batch of B requests x T nodes per step (weak scaling)."""
+    return B * T * world / (ms * 1e-3)
+
+
+def rank_seed(seed: int, rank: int) -> int:
+    """Each rank draws its own batch from its own seed."""
+    return seed + rank
+
+
 # ------------------------------------------------------------------------------------------ algorithmic bytes
 ES = {"f32": 4, "bf16": 2, "e4m3": 1}
 
@@ -396,7 +418,7 @@ def run_sv(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    w = W.make_workload(args.workload, seed=args.seed + rank)
+    w = W.make_workload(args.workload, seed=rank_seed(args.seed, rank))
 
     def to_dev(a, pin=False):
         a = np.ascontiguousarray(a)
@@ -462,12 +484,8 @@ def run_sv(args, rank, world, local_rank):
         dist.barrier()
     t_attn = sum(e0.elapsed_time(e1) for e0, e1, _ in evs) / args.steps
     t_acc = sum(e1.elapsed_time(e2) for _, e1, e2 in evs) / args.steps
-    ms = t_attn + t_acc
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = B * T * world / (ms * 1e-3)
+    ms = max_over_ranks(t_attn + t_acc, world, dev)
+    value = nodes_per_second(B, T, world, ms)
 
     # end to end through the C ABI: inputs from pinned host memory, outputs back, inside the timed region
     e2e = None
@@ -499,12 +517,8 @@ def run_sv(args, rank, world, local_rank):
             e2e_step()
         t1.record(stream)
         torch.cuda.synchronize()
-        ms_e2e = t0.elapsed_time(t1) / n_e2e
-        if world > 1:
-            t = torch.tensor([ms_e2e], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms_e2e = float(t.item())
-        e2e = {"value": B * T * world / (ms_e2e * 1e-3), "unit": "nodes/s", "h2d_bytes_per_step": int(h2d) * world,
+        ms_e2e = max_over_ranks(t0.elapsed_time(t1) / n_e2e, world, dev)
+        e2e = {"value": nodes_per_second(B, T, world, ms_e2e), "unit": "nodes/s", "h2d_bytes_per_step": int(h2d) * world,
                "d2h_bytes_per_step": int(d2h) * world, "ms_per_step": ms_e2e}
 
     if rank != 0:
