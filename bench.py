@@ -6,7 +6,8 @@ A step is one pass of the verify path over one batch: sv_tree_attn over every no
 then sv_accept (walk + bonus).  The default workload is the Llama3-8B-shaped EAGLE tree batch
 (B=8, 60-node trees, 32/8 heads, D=128, bf16, KV prefixes of 2048..8192, vocabulary 128256, greedy).
 value = B*T*world / device time per step (CUDA events on the launching stream, L2 flushed between steps
-by a 256 MB write outside the timed events).  e2e = the same metric through the C ABI with the step's
+by a 256 MB write outside the timed events; each call replayed from a CUDA graph captured after the
+warm-up).  e2e = the same metric through the C ABI with the step's
 inputs copied from pinned host memory and its outputs copied back inside the timed region.  Under
 torchrun every rank verifies its own batch (weak scaling, no collective on the data path).
 --impl reference times the CPU oracle on bounded samples of the same workload.
@@ -450,14 +451,20 @@ def run_sv(args, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
     logits = d["target_logits"]
 
-    def step():
+    def attn_call():
         sv.tree_attn(d["q"], d["k"], d["v"], d["kv_len"], d["parent"], out, k_scale=d.get("k_scale"),
                      v_scale=d.get("v_scale"), lse=lse, status=st_a, workspace=ws_attn)
-        ev_mid = torch.cuda.Event(enable_timing=True)
-        ev_mid.record(stream)
+
+    def accept_call():
         sv.accept(logits, d["tokens"], d["parent"], acc["accept_len"], acc["path"], acc["out_tokens"],
                   acc["bonus"], draft_logits=d["draft_logits"], temperature=w.temperature, uniforms=d["uniforms"],
                   status=acc["status"], workspace=ws_acc)
+
+    def step():
+        attn_call()
+        ev_mid = torch.cuda.Event(enable_timing=True)
+        ev_mid.record(stream)
+        accept_call()
         return ev_mid
 
     for _ in range(args.warmup):
@@ -465,6 +472,33 @@ def run_sv(args, rank, world, local_rank):
         step()
     torch.cuda.synchronize()
     assert (st_a == 0).all() and (acc["status"] == 0).all(), "verify step reported a per-request error"
+
+    # The timed steps replay the two calls as CUDA graphs captured after the warm-up (one graph per call, so
+    # an event still separates attention from acceptance): the device runs the same kernels, without the
+    # host-side launch work of each call in front of them.
+    g_attn, g_acc = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g_attn, stream=side):
+            attn_call()
+        with torch.cuda.graph(g_acc, stream=side):
+            accept_call()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+
+    def graph_step():
+        g_attn.replay()
+        ev_mid = torch.cuda.Event(enable_timing=True)
+        ev_mid.record(stream)
+        g_acc.replay()
+        return ev_mid
+
+    for _ in range(2):
+        flush.zero_()
+        graph_step()
+    torch.cuda.synchronize()
+    assert (st_a == 0).all() and (acc["status"] == 0).all(), "graph-replayed step reported a per-request error"
 
     if world > 1:
         dist.barrier()
@@ -476,7 +510,7 @@ def run_sv(args, rank, world, local_rank):
             e0 = torch.cuda.Event(enable_timing=True)
             e2 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            e1 = step()
+            e1 = graph_step()
             e2.record(stream)
             evs.append((e0, e1, e2))
         torch.cuda.synchronize()
@@ -550,6 +584,7 @@ def run_sv(args, rank, world, local_rank):
             "config": {"workload": args.workload, "B": B, "T": T, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D, "V": V,
                        "kv_dt": w.kv_dt, "logit_dt": w.logit_dt, "mode": w.meta["mode"],
                        "mean_kv_len": float(np.mean(w.kv_len)), "l2": "flushed by a 256 MB write between steps",
+                       "launch": "each call replayed as a CUDA graph captured after the warm-up",
                        "parallelism": f"replicas{world}" if world > 1 else "single"},
             "components": {"attn_ms": t_attn, "accept_ms": t_acc, "attn_bytes": ab, "accept_bytes": cb},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,

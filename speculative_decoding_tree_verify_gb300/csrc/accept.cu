@@ -19,6 +19,7 @@
 //   prefix_sum(j) > floor(U_0 * R / 2^32).
 #include <cooperative_groups.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "sv_internal.cuh"
@@ -867,13 +868,14 @@ __global__ void __launch_bounds__(kWalkThreads, 2) accept_walk_kernel(AcceptArgs
     }
 }
 
+// SM count of the current device (cached per device)
 int sm_count() {
-    static int n = 0;
-    if (!n) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            n = 1;
-    }
+    static std::atomic<int> cached[64] = {};
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (dev >= 0 && dev < 64 && (n = cached[dev].load()) > 0) return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return 1;
+    if (dev >= 0 && dev < 64) cached[dev].store(n);
     return n;
 }
 
@@ -912,14 +914,19 @@ cudaError_t launch_typed(const AcceptArgs& a, cudaStream_t s) {
     const bool staged = stoch && LDT == SV_BF16 && a.V % 8 == 0 && (long long)chunk_s * 2 <= kStoMaxSlice;
     if (staged) {
         const size_t smem = (size_t)chunk_s * 2;
-        static bool attr_set[2] = {false, false};
-        if (!attr_set[a.argmax ? 1 : 0]) {
-            // room for the slice, and the whole unified L1 as shared memory so several CTAs fit on an SM
+        // room for the slice, and the whole unified L1 as shared memory so several CTAs fit on an SM; function
+        // attributes belong to a device, so they are set once per device (and kernel variant)
+        static std::atomic<uint64_t> attr_set[2] = {{0}, {0}};
+        int dev = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+        std::atomic<uint64_t>& done = attr_set[a.argmax ? 1 : 0];
+        if (!bit || !(done.load() & bit)) {
             const void* fn = a.argmax ? (const void*)accept_rows_staged_kernel<true> : (const void*)accept_rows_staged_kernel<false>;
             e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kStoMaxSlice);
             if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
             if (e != cudaSuccess) return e;
-            attr_set[a.argmax ? 1 : 0] = true;
+            done.fetch_or(bit);
         }
         if (a.argmax) e = launch_ex(accept_rows_staged_kernel<true>, dim3(CLs * rows), dim3(kStoThreads), smem, s, CLs, false, a, CLs, chunk_s, rows_src);
         else          e = launch_ex(accept_rows_staged_kernel<false>, dim3(CLs * rows), dim3(kStoThreads), smem, s, CLs, false, a, CLs, chunk_s, rows_src);

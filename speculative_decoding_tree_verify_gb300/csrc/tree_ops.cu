@@ -17,6 +17,8 @@
 //   request ranks the n_front * k candidates by path score and keeps the n_keep best in (slot, rank) order.
 #include <cooperative_groups.h>
 
+#include <atomic>
+
 #include "sv_internal.cuh"
 
 namespace cg = cooperative_groups;
@@ -374,13 +376,14 @@ __global__ void __launch_bounds__(kSelThreads) expand_select_kernel(ExpandArgs a
     if (tid == 0 && a.status) a.status[b] = SV_OK;
 }
 
+// SM count of the current device (cached per device)
 int expand_sm_count() {
-    static int n = 0;
-    if (!n) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            n = 1;
-    }
+    static std::atomic<int> cached[64] = {};
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (dev >= 0 && dev < 64 && (n = cached[dev].load()) > 0) return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return 1;
+    if (dev >= 0 && dev < 64) cached[dev].store(n);
     return n;
 }
 
