@@ -428,7 +428,7 @@ def expansion_levels(T: int, branching) -> list[tuple[int, int, int]]:
 
 
 # ----------------------------------------------------------------------------------------------------
-# named workloads (the shapes of the pages' serving setups; see the design doc for the recipe)
+# named workloads (the shapes of the pages' serving setups, with the recipe of the generators above)
 # ----------------------------------------------------------------------------------------------------
 WORKLOADS = {
     # B=1, chain of 5 drafts, 4/1 heads, D=64, fp32 QKV, L=128, fp32 logits V=1024, greedy
