@@ -326,6 +326,19 @@ def run_ops(args):
                           "frac": round(tf / peak_alu, 3), "bound": "alu", "peak_TFLOP_s": round(peak_alu, 1),
                           "note": "CUDA cores, fp32; FLOPs = 10*D per (query row, allowed position)"}), flush=True)
 
+    def paged_case(name, w, page_size=128):
+        """Tree attention over the same caches scattered into a page pool (CUDA-core kernel); bytes as for
+        the contiguous call."""
+        kp, table = W.to_pages(args.seed, w.k, w.kv_len, w.T, page_size)
+        vp, _ = W.to_pages(args.seed, w.v, w.kv_len, w.T, page_size)
+        q, kpd, vpd, tbl = dev(w.q), dev(kp), dev(vp), dev(table)
+        kl, par, ks, vs = dev(w.kv_len), dev(w.parent), dev(w.k_scale), dev(w.v_scale)
+        out = torch.empty_like(q)
+        lse = torch.empty((w.B, w.T, w.Hq), dtype=torch.float32, device="cuda")
+        st = torch.empty((w.B,), **i32)
+        fn = lambda: sv.tree_attn_paged(q, kpd, vpd, tbl, kl, par, out, k_scale=ks, v_scale=vs, lse=lse, status=st)
+        report(name, "tree_attn_paged", timed(fn, reps=5), attn_bytes(w), f"CUDA cores, {page_size}-row pages")
+
     def compact_case(name, B, T, Hkv, D, kv_cap, kv_dt, kv_len, parent, seed):
         """KV compaction of random accepted root paths; bytes = the moved rows read once and written once."""
         shape = (B, Hkv, kv_cap, D)
@@ -380,6 +393,7 @@ def run_ops(args):
         accept_case(name, w, w.temperature, w.draft_logits if w.temperature > 0 else None)
         if name in ("llama3_8b_tree", "qwen3_8b_stochastic"):
             bwd_case(name, w)
+            paged_case(name, w)
         compact_case(name, w.B, w.T, w.Hkv, w.D, w.kv_cap, w.kv_dt, w.kv_len, w.parent, args.seed)
         if name == "llama3_8b_tree":
             expand_case(name, w.B, w.V, W.expansion_levels(60, (4, 3, 2, 2, 1, 1)), 3.0, 200 + args.seed)
