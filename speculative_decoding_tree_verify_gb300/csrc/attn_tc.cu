@@ -19,7 +19,7 @@
 // second kernel, attn_merge_kernel, merges them, validates every request and writes the status array.
 //
 // Roles in one CTA of attn_tc_kernel (persistent, 12 warps):
-//   warps 0, 3   TMA producers (bf16 caches): warp 0 loads the K tiles into a 3-slot K ring, warp 3 the V
+//   warps 0, 3   TMA producers (bf16 caches): warp 0 loads the K tiles into a 2-slot K ring, warp 3 the V
 //                tiles into a 2-slot V ring (128 x 128 bf16 as two 64-column boxes, 128-byte swizzle), so
 //                K tiles, released as soon as S is computed, run ahead of the V tiles held until the PV.
 //                e4m3 caches: warp 0 loads both into a staging ring and warp 3 converts them to f16.
