@@ -4,9 +4,11 @@
 // acceptance length is the number of draft tokens accepted per verification step (TIDE evaluation).
 //
 // Kernel 1 (rows): one thread-block cluster of CL CTAs per logit row, each CTA one contiguous slice of
-//   the vocabulary, 128-bit loads.  Greedy: (max, first index) -> argmax.  Stochastic: max of y = z*invT,
-//   then the fixed-point weight sum S of the integer contract.  Partial results meet in distributed
-//   shared memory; no global partials, one HBM read of every row.
+//   the vocabulary, 128-bit loads.  Greedy: (max, first index) -> argmax.  Stochastic (fp32 rows, or rows
+//   whose length breaks 16-byte alignment): max of y = z*invT, then the fixed-point weight sum S of the
+//   integer contract over a second, cache-served pass.  Partial results meet in distributed shared memory.
+// Kernel 1b (staged rows, stochastic bf16): each CTA bulk-copies its slice into shared memory, so the row
+//   is read from HBM once, and computes max / min and then the weights from there.
 // Kernel 2 (walk): one cluster per request.  Greedy: a single thread follows the argmax matches.
 //   Stochastic: every thread of the cluster runs the same walk on broadcast scalars; the residual sums and
 //   the bonus draw are cluster-wide passes over the stopping row only.
