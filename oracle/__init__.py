@@ -81,6 +81,7 @@ def load(path):
     L.or_kv_compact.argtypes = [i, i, i, i, i, i, P, P, P, P, P, P, P, P]
     L.or_tree_expand.argtypes = [i, i, i, i, i, i, P, P, P, P, P, P, P, P]
     L.or_tree_attn_bwd.argtypes = [i, i, i, i, i, i, i, i, P, P, P, P, P, C.c_double, P, P, P, P, P]
+    L.or_tree_attn_e2m1.argtypes = [i, i, i, i, i, i, i, P, P, P, P, P, P, P, P, P, C.c_double, P, P, P]
     return L
 
 
@@ -135,6 +136,27 @@ def tree_attn_w(w, rows=None, sm_scale=0.0):
     """tree_attn on a workloads.Verify batch."""
     return tree_attn(w.q, w.k, w.v, w.kv_len, w.parent, Hq=w.Hq, Hkv=w.Hkv, q_dt=w.q_dt, kv_dt=w.kv_dt,
                      k_scale=w.k_scale, v_scale=w.v_scale, sm_scale=sm_scale, rows=rows)
+
+
+def tree_attn_e2m1(q, k_codes, v_codes, k_block, v_block, k_scale, v_scale, kv_len, parent, *, Hq, q_dt,
+                   sm_scale=0.0):
+    """Tree attention over FP4 (E2M1) caches with E4M3 block scales (16 elements) and fp32 head scales.
+    k_codes / v_codes [B, Hkv, kv_cap, D/2] uint8 (even element in the low nibble).  Returns (out, lse,
+    status, rc) like tree_attn."""
+    q = np.ascontiguousarray(q)
+    B, T = parent.shape
+    D = q.shape[-1]
+    Hkv, kv_cap = k_codes.shape[1], k_codes.shape[2]
+    out = np.full((B, T, Hq, D), np.nan)
+    lse = np.full((B, T, Hq), np.nan)
+    status = np.zeros(B, np.int32)
+    args = [np.ascontiguousarray(x, np.uint8) for x in (k_codes, v_codes, k_block, v_block)]
+    ks = np.ascontiguousarray(k_scale, np.float32)
+    vs = np.ascontiguousarray(v_scale, np.float32)
+    rc = lib().or_tree_attn_e2m1(B, T, Hq, Hkv, D, kv_cap, DT[q_dt], _p(q), *[_p(x) for x in args], _p(ks), _p(vs),
+                                 _p(np.ascontiguousarray(kv_len, np.int32)), _p(np.ascontiguousarray(parent, np.int32)),
+                                 float(sm_scale), _p(out), _p(lse), _p(status))
+    return out, lse, status, rc
 
 
 def tree_attn_paged(q, k_pool, v_pool, page_table, kv_len, parent, *, Hq, Hkv, q_dt, kv_dt, k_scale=None,

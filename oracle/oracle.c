@@ -31,7 +31,7 @@
 typedef unsigned __int128 u128;
 
 enum { OK = 0, E_ARG = 1, E_TREE = 2, E_BIG = 3, E_UNSUP = 4, E_NONFINITE = 5 };
-enum { DT_F32 = 0, DT_BF16 = 1, DT_E4M3 = 2 };
+enum { DT_F32 = 0, DT_BF16 = 1, DT_E4M3 = 2, DT_F64_DECODED = 9 /* internal: caches decoded to float64 */ };
 
 int or_num_threads(void) {
 #ifdef _OPENMP
@@ -66,6 +66,7 @@ static double load_elem(const void* base, size_t i, int dt) {
     switch (dt) {
     case DT_F32:  return (double)((const float*)base)[i];
     case DT_BF16: return (double)bf16_to_float(((const uint16_t*)base)[i]);
+    case DT_F64_DECODED: return ((const double*)base)[i];
     default:      return e4m3_to_double(((const uint8_t*)base)[i]);
     }
 }
@@ -712,5 +713,61 @@ int or_tree_attn_bwd(int B, int T, int Hq, int Hkv, int D, int kv_cap, int q_dt,
                              scale, b, i, h, dqr, dk, dv);
             }
     }
+    return OK;
+}
+
+
+/* ---------------------------------------------------------------------------------------------- */
+/* FP4 (e2m1) KV caches                                                                             */
+/* ---------------------------------------------------------------------------------------------- */
+/* OCP 4-bit floating point E2M1: 1 sign, 2 exponent bits (bias 1), 1 mantissa bit, no infinities or NaN:
+ * magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6.  A cache element is code * block scale * head scale, with one
+ * E4M3 block scale per 16 consecutive elements of a row (the NVFP4 layout) and the fp32 per-kv-head scale of
+ * the E4M3 caches.  Codes are packed two per byte, the even element in the low nibble. */
+static double e2m1_to_double(unsigned c) {
+    int e = (c >> 1) & 3, m = c & 1;
+    double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return (c & 8) ? -v : v;
+}
+
+/* Tree attention over FP4 caches: k / v codes [B, Hkv, kv_cap, D/2] bytes, block scales [B, Hkv, kv_cap,
+ * D/16] E4M3 codes, head scales [Hkv] fp32.  The caches are decoded to float64 and the plain definition
+ * above runs on them.  D must be a multiple of 16. */
+int or_tree_attn_e2m1(int B, int T, int Hq, int Hkv, int D, int kv_cap, int q_dt, const void* q,
+                      const uint8_t* k, const uint8_t* v, const uint8_t* k_block, const uint8_t* v_block,
+                      const float* k_scale, const float* v_scale, const int32_t* kv_len, const int32_t* parent,
+                      double sm_scale, double* out, double* lse, int32_t* status) {
+    if (B < 0 || T < 1 || Hq < 1 || Hkv < 1 || D < 16 || D % 16 || kv_cap < 0) return E_ARG;
+    if (T > 64) return E_BIG;
+    if (Hq % Hkv) return E_ARG;
+    if (q_dt != DT_F32 && q_dt != DT_BF16) return E_UNSUP;
+    size_t n = (size_t)B * Hkv * kv_cap * D;
+    double* kd = (double*)malloc(sizeof(double) * n);
+    double* vd = (double*)malloc(sizeof(double) * n);
+    for (size_t i = 0; i < n; ++i) {
+        size_t row = i / (size_t)D;
+        int h = (int)(row / (size_t)kv_cap % (size_t)Hkv);
+        size_t blk = row * (size_t)(D / 16) + (i % (size_t)D) / 16;
+        unsigned kc = (k[i / 2] >> (4 * (i & 1))) & 15, vc = (v[i / 2] >> (4 * (i & 1))) & 15;
+        kd[i] = e2m1_to_double(kc) * e4m3_to_double(k_block[blk]) * (double)k_scale[h];
+        vd[i] = e2m1_to_double(vc) * e4m3_to_double(v_block[blk]) * (double)v_scale[h];
+    }
+    double scale = sm_scale != 0.0 ? sm_scale : 1.0 / sqrt((double)D);
+    for (int b = 0; b < B; ++b) {
+        int st = or_tree_check(T, parent + (size_t)b * T);
+        if (!st && (kv_len[b] < 0 || kv_len[b] + T > kv_cap)) st = E_ARG;
+        status[b] = st;
+    }
+    long total = (long)B * T * Hq;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (long r = 0; r < total; ++r) {
+        int h = (int)(r % Hq), i = (int)((r / Hq) % T), b = (int)(r / ((long)Hq * T));
+        if (status[b]) continue;
+        size_t idx = ((size_t)b * T + i) * Hq + h;
+        attn_row(T, Hq, Hkv, D, kv_cap, q_dt, DT_F64_DECODED, q, kd, vd, NULL, NULL, kv_len[b],
+                 parent + (size_t)b * T, scale, b, i, h, out + idx * D, lse + idx);
+    }
+    free(kd);
+    free(vd);
     return OK;
 }

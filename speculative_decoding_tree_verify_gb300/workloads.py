@@ -75,6 +75,46 @@ def f32_to_e4m3(x) -> np.ndarray:
     return (code | np.where(x < 0, 0x80, 0)).astype(np.uint8)
 
 
+# OCP E2M1 magnitudes by code 0..7 (sign in bit 3)
+E2M1_POS = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def f32_to_e2m1_codes(x) -> np.ndarray:
+    """float -> E2M1 codes 0..15, round to nearest (ties to the even code), saturating at +-6."""
+    x = np.asarray(x, np.float64)
+    a = np.abs(x)
+    hi = np.clip(np.searchsorted(E2M1_POS, a, side="left"), 1, 7)
+    lo = hi - 1
+    d_lo = a - E2M1_POS[lo]
+    d_hi = E2M1_POS[hi] - a
+    code = np.where((d_lo < d_hi) | ((d_lo == d_hi) & (lo % 2 == 0)), lo, hi)
+    code = np.where(a >= 6.0, 7, code)
+    return (code | np.where(x < 0, 8, 0)).astype(np.uint8)
+
+
+def encode_nvfp4(x, pow2_head_scale: bool = False):
+    """A float32 cache [B, Hkv, cap, D] (D a multiple of 16) -> (codes [B,Hkv,cap,D/2] with the even element in
+    the low nibble, E4M3 block scales [B,Hkv,cap,D/16], fp32 head scales [Hkv]).  Head scale
+    amax / (6 * 448) (or the next power of two above it), block scale = E4M3(block amax / 6 / head scale), codes =
+    E2M1(x / (block * head)).  Data encoding only."""
+    x = np.asarray(x, np.float32)
+    B, H, cap, D = x.shape
+    amax = np.maximum(np.abs(x).max(axis=(0, 2, 3)).astype(np.float64), 1e-30)
+    hs = amax / (6.0 * 448.0)
+    if pow2_head_scale:
+        hs = 2.0 ** np.ceil(np.log2(hs))
+    hs = hs.astype(np.float32)
+    blocks = x.reshape(B, H, cap, D // 16, 16).astype(np.float64)
+    bamax = np.abs(blocks).max(axis=-1)
+    bcode = f32_to_e4m3(bamax / 6.0 / hs[None, :, None, None].astype(np.float64))
+    bval = _E4M3_POS[np.minimum(bcode & 0x7F, 126)]
+    denom = bval[..., None] * hs[None, :, None, None, None].astype(np.float64)
+    q = np.where(denom > 0, blocks / np.where(denom > 0, denom, 1.0), 0.0)
+    codes = f32_to_e2m1_codes(q).reshape(B, H, cap, D)
+    packed = (codes[..., 0::2] | (codes[..., 1::2] << 4)).astype(np.uint8)
+    return packed, bcode.astype(np.uint8), hs
+
+
 def encode(x, dt: str) -> np.ndarray:
     if dt == "f32":
         return np.ascontiguousarray(x, dtype=np.float32)

@@ -15,6 +15,7 @@ from tests import test_oracle_attn as TT
 from tests import test_oracle_attn_bwd as TB
 from tests import test_oracle_compact as TC
 from tests import test_oracle_expand as TE
+from tests import test_oracle_fp4 as TF
 from tests import test_oracle_loss as TL
 
 MUTANTS = {
@@ -57,6 +58,9 @@ MUTANTS = {
     "attn_bwd_value_grad_uses_q": (
         "dv[row * D + d] += p * g[d];", "dv[row * D + d] += p * qv[d];",
         TB.test_backward_matches_central_finite_differences),
+    "fp4_high_nibble_first": (
+        "unsigned kc = (k[i / 2] >> (4 * (i & 1))) & 15,", "unsigned kc = (k[i / 2] >> (4 * (1 - (i & 1)))) & 15,",
+        lambda: TF.test_fp4_attention_equals_attention_on_independently_decoded_caches((3, 2, 2), 13)),
     "fx_poly_drops_cubic": (
         "p = fmaf(p, f, C_P3);", "p = fmaf(p, f, 0.0f);", TA.test_fx_exp2_polynomial_error_bound),
 }
