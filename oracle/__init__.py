@@ -81,7 +81,9 @@ def load(path):
     L.or_kv_compact.argtypes = [i, i, i, i, i, i, P, P, P, P, P, P, P, P]
     L.or_tree_expand.argtypes = [i, i, i, i, i, i, P, P, P, P, P, P, P, P]
     L.or_tree_attn_bwd.argtypes = [i, i, i, i, i, i, i, i, P, P, P, P, P, C.c_double, P, P, P, P, P]
-    L.or_tree_attn_e2m1.argtypes = [i, i, i, i, i, i, i, P, P, P, P, P, P, P, P, P, C.c_double, P, P, P]
+    L.or_tree_attn_e2m1.argtypes = [i, i, i, i, i, i, i, P, P, P, P, P, P, P, P, P, C.c_double, P, i, P, P, P]
+    L.or_set_num_threads.argtypes = [i]
+    L.or_set_num_threads.restype = None
     return L
 
 
@@ -91,6 +93,11 @@ def _p(a):
 
 def num_threads() -> int:
     return int(lib().or_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Thread count of later oracle calls (OpenMP)."""
+    lib().or_set_num_threads(int(n))
 
 
 # ------------------------------------------------------------------------------------------------ tree
@@ -139,10 +146,10 @@ def tree_attn_w(w, rows=None, sm_scale=0.0):
 
 
 def tree_attn_e2m1(q, k_codes, v_codes, k_block, v_block, k_scale, v_scale, kv_len, parent, *, Hq, q_dt,
-                   sm_scale=0.0):
+                   sm_scale=0.0, rows=None):
     """Tree attention over FP4 (E2M1) caches with E4M3 block scales (16 elements) and fp32 head scales.
     k_codes / v_codes [B, Hkv, kv_cap, D/2] uint8 (even element in the low nibble).  Returns (out, lse,
-    status, rc) like tree_attn."""
+    status, rc) like tree_attn; rows: optional (b, i, h) triples to compute, other entries stay NaN."""
     q = np.ascontiguousarray(q)
     B, T = parent.shape
     D = q.shape[-1]
@@ -153,9 +160,10 @@ def tree_attn_e2m1(q, k_codes, v_codes, k_block, v_block, k_scale, v_scale, kv_l
     args = [np.ascontiguousarray(x, np.uint8) for x in (k_codes, v_codes, k_block, v_block)]
     ks = np.ascontiguousarray(k_scale, np.float32)
     vs = np.ascontiguousarray(v_scale, np.float32)
+    r = None if rows is None else np.ascontiguousarray(np.unique(np.asarray(rows, np.int32).reshape(-1, 3), axis=0))
     rc = lib().or_tree_attn_e2m1(B, T, Hq, Hkv, D, kv_cap, DT[q_dt], _p(q), *[_p(x) for x in args], _p(ks), _p(vs),
                                  _p(np.ascontiguousarray(kv_len, np.int32)), _p(np.ascontiguousarray(parent, np.int32)),
-                                 float(sm_scale), _p(out), _p(lse), _p(status))
+                                 float(sm_scale), _p(r), 0 if r is None else len(r), _p(out), _p(lse), _p(status))
     return out, lse, status, rc
 
 

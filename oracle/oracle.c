@@ -30,7 +30,7 @@
 
 typedef unsigned __int128 u128;
 
-enum { OK = 0, E_ARG = 1, E_TREE = 2, E_BIG = 3, E_UNSUP = 4, E_NONFINITE = 5 };
+enum { OK = 0, E_ARG = 1, E_TREE = 2, E_BIG = 3, E_UNSUP = 4, E_NONFINITE = 5, E_NOMEM = 9 };
 enum { DT_F32 = 0, DT_BF16 = 1, DT_E4M3 = 2, DT_F64_DECODED = 9 /* internal: caches decoded to float64 */ };
 
 int or_num_threads(void) {
@@ -38,6 +38,14 @@ int or_num_threads(void) {
     return omp_get_max_threads();
 #else
     return 1;
+#endif
+}
+
+void or_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
 #endif
 }
 
@@ -731,41 +739,61 @@ static double e2m1_to_double(unsigned c) {
 }
 
 /* Tree attention over FP4 caches: k / v codes [B, Hkv, kv_cap, D/2] bytes, block scales [B, Hkv, kv_cap,
- * D/16] E4M3 codes, head scales [Hkv] fp32.  The caches are decoded to float64 and the plain definition
- * above runs on them.  D must be a multiple of 16. */
+ * D/16] E4M3 codes, head scales [Hkv] fp32.  Each request's caches are decoded to float64 (one request at a
+ * time, so memory stays at one request's worth) and the plain definition above runs on them.  rows, if
+ * given, lists the (b, i, h) triples to compute (n_rows of them, grouped by b in any order); other outputs
+ * are left untouched.  D must be a multiple of 16.  Returns E_NOMEM if the decode buffers cannot be had. */
 int or_tree_attn_e2m1(int B, int T, int Hq, int Hkv, int D, int kv_cap, int q_dt, const void* q,
                       const uint8_t* k, const uint8_t* v, const uint8_t* k_block, const uint8_t* v_block,
                       const float* k_scale, const float* v_scale, const int32_t* kv_len, const int32_t* parent,
-                      double sm_scale, double* out, double* lse, int32_t* status) {
+                      double sm_scale, const int32_t* rows, int n_rows, double* out, double* lse, int32_t* status) {
     if (B < 0 || T < 1 || Hq < 1 || Hkv < 1 || D < 16 || D % 16 || kv_cap < 0) return E_ARG;
     if (T > 64) return E_BIG;
     if (Hq % Hkv) return E_ARG;
     if (q_dt != DT_F32 && q_dt != DT_BF16) return E_UNSUP;
-    size_t n = (size_t)B * Hkv * kv_cap * D;
-    double* kd = (double*)malloc(sizeof(double) * n);
-    double* vd = (double*)malloc(sizeof(double) * n);
-    for (size_t i = 0; i < n; ++i) {
-        size_t row = i / (size_t)D;
-        int h = (int)(row / (size_t)kv_cap % (size_t)Hkv);
-        size_t blk = row * (size_t)(D / 16) + (i % (size_t)D) / 16;
-        unsigned kc = (k[i / 2] >> (4 * (i & 1))) & 15, vc = (v[i / 2] >> (4 * (i & 1))) & 15;
-        kd[i] = e2m1_to_double(kc) * e4m3_to_double(k_block[blk]) * (double)k_scale[h];
-        vd[i] = e2m1_to_double(vc) * e4m3_to_double(v_block[blk]) * (double)v_scale[h];
-    }
     double scale = sm_scale != 0.0 ? sm_scale : 1.0 / sqrt((double)D);
     for (int b = 0; b < B; ++b) {
         int st = or_tree_check(T, parent + (size_t)b * T);
         if (!st && (kv_len[b] < 0 || kv_len[b] + T > kv_cap)) st = E_ARG;
         status[b] = st;
     }
-    long total = (long)B * T * Hq;
-#pragma omp parallel for schedule(dynamic, 4)
-    for (long r = 0; r < total; ++r) {
-        int h = (int)(r % Hq), i = (int)((r / Hq) % T), b = (int)(r / ((long)Hq * T));
+    size_t n = (size_t)Hkv * kv_cap * D;                 /* one request's elements per cache */
+    double* kd = (double*)malloc(sizeof(double) * (n ? n : 1));
+    double* vd = (double*)malloc(sizeof(double) * (n ? n : 1));
+    if (!kd || !vd) {
+        free(kd);
+        free(vd);
+        return E_NOMEM;
+    }
+    size_t qsz = q_dt == DT_F32 ? 4 : 2;
+    for (int b = 0; b < B; ++b) {
         if (status[b]) continue;
-        size_t idx = ((size_t)b * T + i) * Hq + h;
-        attn_row(T, Hq, Hkv, D, kv_cap, q_dt, DT_F64_DECODED, q, kd, vd, NULL, NULL, kv_len[b],
-                 parent + (size_t)b * T, scale, b, i, h, out + idx * D, lse + idx);
+        int wanted = rows == NULL;
+        for (int r = 0; r < n_rows && !wanted; ++r) wanted = rows[3 * r] == b;
+        if (!wanted) continue;
+        size_t base = (size_t)b * n;
+        for (size_t i = 0; i < n; ++i) {
+            size_t row = i / (size_t)D;                  /* (kv head, position) row inside the request */
+            int h = (int)(row / (size_t)kv_cap);
+            size_t blk = (base + i) / 16;                /* 16 consecutive elements of a row share a scale */
+            unsigned kc = (k[(base + i) / 2] >> (4 * (i & 1))) & 15, vc = (v[(base + i) / 2] >> (4 * (i & 1))) & 15;
+            kd[i] = e2m1_to_double(kc) * e4m3_to_double(k_block[blk]) * (double)k_scale[h];
+            vd[i] = e2m1_to_double(vc) * e4m3_to_double(v_block[blk]) * (double)v_scale[h];
+        }
+        const void* qb = (const char*)q + (size_t)b * T * Hq * D * qsz;
+        long total = (long)T * Hq;
+#pragma omp parallel for schedule(dynamic, 4)
+        for (long r = 0; r < total; ++r) {
+            int h = (int)(r % Hq), i = (int)(r / Hq);
+            if (rows) {
+                int hit = 0;
+                for (int x = 0; x < n_rows && !hit; ++x) hit = rows[3 * x] == b && rows[3 * x + 1] == i && rows[3 * x + 2] == h;
+                if (!hit) continue;
+            }
+            size_t idx = ((size_t)b * T + i) * Hq + h;
+            attn_row(T, Hq, Hkv, D, kv_cap, q_dt, DT_F64_DECODED, qb, kd, vd, NULL, NULL, kv_len[b],
+                     parent + (size_t)b * T, scale, 0, i, h, out + idx * D, lse + idx);
+        }
     }
     free(kd);
     free(vd);

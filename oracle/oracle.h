@@ -77,14 +77,19 @@ int or_tree_attn_bwd(int B, int T, int Hq, int Hkv, int D, int kv_cap, int q_dt,
 
 /* Tree attention over FP4 caches (OCP E2M1 codes, two per byte, even element in the low nibble), one E4M3
  * block scale per 16 elements of a row and an fp32 scale per kv head: value = code * block * head scale.
- * k / v [B, Hkv, kv_cap, D/2] bytes, k_block / v_block [B, Hkv, kv_cap, D/16], k_scale / v_scale [Hkv]. */
+ * k / v [B, Hkv, kv_cap, D/2] bytes, k_block / v_block [B, Hkv, kv_cap, D/16], k_scale / v_scale [Hkv].
+ * rows: NULL (every row) or n_rows (b, i, h) triples.  Returns 9 if memory for one request's decoded
+ * caches cannot be allocated. */
 int or_tree_attn_e2m1(int B, int T, int Hq, int Hkv, int D, int kv_cap, int q_dt, const void* q,
                       const uint8_t* k, const uint8_t* v, const uint8_t* k_block, const uint8_t* v_block,
                       const float* k_scale, const float* v_scale, const int32_t* kv_len, const int32_t* parent,
-                      double sm_scale, double* out, double* lse, int32_t* status);
+                      double sm_scale, const int32_t* rows, int n_rows, double* out, double* lse, int32_t* status);
 
 /* Number of OpenMP threads the oracle will use (1 when built without OpenMP). */
 int or_num_threads(void);
+
+/* Set the number of OpenMP threads of later calls (no effect without OpenMP or for n < 1). */
+void or_set_num_threads(int n);
 
 #ifdef __cplusplus
 }

@@ -234,6 +234,29 @@ def _force_max(row_f32: np.ndarray, tok: int) -> float:
     return float(np.max(row_f32)) + 1.0
 
 
+def _draft_tokens(parents: np.ndarray, tokens: np.ndarray, V: int, force_p: float, s_tok, s_force):
+    """Greedy / one-hot draft tokens, written into tokens[:, 1:]: the children of every internal node get
+    distinct random tokens; with probability force_p one uniformly chosen child's token is the one the
+    target row of the parent is made to peak at, otherwise a token outside the children is.  Returns the
+    (request, parent node, peak token) triples, in the order the streams were drawn."""
+    B, T = parents.shape
+    peaks = []
+    for b in range(B):
+        ch = children_of(parents[b])
+        for p in range(T):
+            if not ch[p]:
+                continue
+            toks = s_tok.choice(V, size=len(ch[p]) + 1, replace=False)
+            for c, x in zip(ch[p], toks[:-1]):
+                tokens[b, c] = x
+            if s_force.random() < force_p:
+                star = int(tokens[b, ch[p][s_force.integers(0, len(ch[p]))]])
+            else:
+                star = int(toks[-1])
+            peaks.append((b, p, star))
+    return peaks
+
+
 def make_verify(seed: int, *, B: int, T: int, Hq: int, Hkv: int, D: int, L: tuple[int, int], V: int,
                 q_dt: str = "bf16", kv_dt: str = "bf16", logit_dt: str = "bf16", tree="chain",
                 mode: str = "greedy", temperature: float = 0.0, force_p: float = 0.7, sigma: float = 3.0,
@@ -294,19 +317,8 @@ def make_verify(seed: int, *, B: int, T: int, Hq: int, Hkv: int, D: int, L: tupl
         zf = (sigma * s_lp.standard_normal(size=(B, T, V), dtype=np.float32))
         target = encode(zf, logit_dt)
         tf = decode_f32(target, logit_dt).copy()
-        for b in range(B):
-            ch = children_of(parents[b])
-            for p in range(T):
-                if not ch[p]:
-                    continue
-                toks = s_tok.choice(V, size=len(ch[p]) + 1, replace=False)
-                for c, x in zip(ch[p], toks[:-1]):
-                    tokens[b, c] = x
-                if s_force.random() < force_p:
-                    star = int(tokens[b, ch[p][s_force.integers(0, len(ch[p]))]])
-                else:
-                    star = int(toks[-1])
-                tf[b, p, star] = _force_max(tf[b, p], star)
+        for b, p, star in _draft_tokens(parents, tokens, V, force_p, s_tok, s_force):
+            tf[b, p, star] = _force_max(tf[b, p], star)
         target = encode(tf, logit_dt)
         del tf, zf
     if mode in ("prob", "onehot"):
@@ -316,6 +328,113 @@ def make_verify(seed: int, *, B: int, T: int, Hq: int, Hkv: int, D: int, L: tupl
                   parent=parents, tokens=tokens, target_logits=target, draft_logits=draft,
                   uniforms=uniforms, temperature=float(temperature if mode != "greedy" else 0.0),
                   name=name, meta=dict(mode=mode, tree=tree, L=L, seed=seed))
+
+
+# ----------------------------------------------------------------------------------------------------
+# verify workloads drawn on the GPU (full-size batches whose caches and logits are too large to draw
+# on the host in reasonable time)
+# ----------------------------------------------------------------------------------------------------
+def _torch_gen(seq: np.random.SeedSequence, device):
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seq.generate_state(1, np.uint64)[0] & 0x7FFFFFFFFFFFFFFF))
+    return g
+
+
+def make_verify_device(seed: int, *, B: int, T: int, Hq: int, Hkv: int, D: int, L: tuple[int, int], V: int,
+                       q_dt: str = "bf16", kv_dt: str = "e4m3", logit_dt: str = "bf16", tree="chain",
+                       mode: str = "greedy", temperature: float = 0.0, force_p: float = 0.7, sigma: float = 3.0,
+                       kv_cap: int | None = None, name: str = "", with_attn: bool = True, device="cuda",
+                       **_ignored) -> Verify:
+    """The greedy / one-hot recipe of make_verify with the large tensors drawn on the GPU.
+
+    The tree, the prefix lengths, the draft tokens, the forced peaks and the uniforms come from the same
+    numpy streams as make_verify (so they are identical to the host recipe's).  Q, the caches and the target
+    logits are drawn with torch's CUDA generator from their own child seeds:
+      * Q ~ N(0,1) rounded to bf16;
+      * K, V ~ N(0,1); e4m3 caches use the per-kv-head amax scale over the valid positions (< kv_len + T),
+        codes by torch's float8_e4m3fn conversion of x / scale clamped to +-448; bf16 caches round x;
+      * target logits sigma * N(0,1) rounded to bf16; at each internal node the peak token's logit is set
+        to the row's maximum + 1 (in float32, then rounded to bf16), as in the host recipe.
+    The returned Verify holds torch CUDA tensors in q, k, v, k_scale, v_scale and target_logits (bf16 bits
+    as int16, e4m3 codes as uint8) and numpy arrays in kv_len, parent, tokens and uniforms.  Use
+    host_requests() to copy a few requests to numpy for the oracle."""
+    import torch
+    if mode not in ("greedy", "onehot") or q_dt != "bf16" or logit_dt != "bf16" or kv_dt not in ("bf16", "e4m3"):
+        raise ValueError("the device recipe covers greedy / one-hot batches with bf16 Q and logits")
+    (s_tree, s_len, s_q, s_k, s_v, s_lp, s_lq, s_tok, s_u, s_force, s_junk) = rng_streams(seed, 11)
+    seqs = np.random.SeedSequence(seed).spawn(11)
+    if tree == "chain":
+        parents = np.stack([chain_tree(T) for _ in range(B)])
+    elif tree == "star":
+        parents = np.stack([star_tree(T) for _ in range(B)])
+    else:
+        parents = np.stack([make_tree(s_tree, T, tree) for _ in range(B)])
+    lo, hi = L
+    kv_len = s_len.integers(lo, hi, size=B, endpoint=True).astype(np.int32)
+    cap = int(kv_cap if kv_cap is not None else hi + T)
+    q = k = v = k_scale = v_scale = None
+    if with_attn:
+        gq = _torch_gen(seqs[2], device)
+        q = torch.randn((B, T, Hq, D), generator=gq, device=device).to(torch.bfloat16).view(torch.int16)
+        valid = (torch.arange(cap, device=device)[None, :] < torch.as_tensor(kv_len, device=device)[:, None] + T)
+        caches, scales = [], []
+        for seq in (seqs[3], seqs[4]):
+            g = _torch_gen(seq, device)
+            c = torch.empty((B, Hkv, cap, D), dtype=torch.uint8 if kv_dt == "e4m3" else torch.int16, device=device)
+            sc = torch.ones(Hkv, dtype=torch.float32, device=device)
+            for h in range(Hkv):          # one kv head at a time bounds the float32 temporary
+                x = torch.randn((B, cap, D), generator=g, device=device)
+                if kv_dt == "e4m3":
+                    amax = torch.where(valid[:, :, None], x.abs(), torch.zeros((), device=device)).amax()
+                    sc[h] = torch.clamp(amax, min=1e-30) / 448.0
+                    c[:, h] = (x / sc[h]).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+                else:
+                    c[:, h] = x.to(torch.bfloat16).view(torch.int16)
+                del x
+            caches.append(c)
+            scales.append(sc if kv_dt == "e4m3" else None)
+        k, v = caches
+        k_scale, v_scale = scales
+    tokens = np.zeros((B, T), np.int32)
+    tokens[:, 0] = s_tok.integers(0, V, size=B)
+    peaks = _draft_tokens(parents, tokens, V, force_p, s_tok, s_force)
+    gz = _torch_gen(seqs[5], device)
+    target = (sigma * torch.randn((B, T, V), generator=gz, device=device)).to(torch.bfloat16)
+    if peaks:
+        bi, pi, ti = (torch.as_tensor(np.array(x, np.int64), device=device) for x in zip(*peaks))
+        rmax = target[bi, pi].float().amax(dim=-1)
+        target[bi, pi, ti] = (rmax + 1.0).to(torch.bfloat16)
+    target = target.view(torch.int16)
+    uniforms = s_u.integers(0, 2 ** 32, size=(B, T), dtype=np.uint32) if mode == "onehot" else None
+    return Verify(B=B, T=T, Hq=Hq, Hkv=Hkv, D=D, kv_cap=cap, V=V, q_dt=q_dt, kv_dt=kv_dt, logit_dt=logit_dt,
+                  q=q, k=k, v=v, k_scale=k_scale, v_scale=v_scale, kv_len=kv_len, parent=parents, tokens=tokens,
+                  target_logits=target, draft_logits=None, uniforms=uniforms,
+                  temperature=float(temperature if mode != "greedy" else 0.0), name=name,
+                  meta=dict(mode=mode, tree=tree, L=L, seed=seed, device_recipe=True))
+
+
+def host_requests(w: Verify, reqs, with_logits: bool = True) -> Verify:
+    """The requests `reqs` of a batch drawn by make_verify_device, copied to numpy in the host encodings
+    (bf16 as uint16 bits, e4m3 as uint8 codes), as a Verify of len(reqs) requests."""
+    import torch
+    idx = torch.as_tensor(np.asarray(reqs, np.int64), device=w.target_logits.device)
+
+    def take(t, view=None):
+        if t is None:
+            return None
+        a = t.index_select(0, idx).cpu().numpy()
+        return a.view(np.uint16) if a.dtype == np.int16 else a
+
+    r = np.asarray(reqs, np.int64)
+    return Verify(B=len(r), T=w.T, Hq=w.Hq, Hkv=w.Hkv, D=w.D, kv_cap=w.kv_cap, V=w.V, q_dt=w.q_dt, kv_dt=w.kv_dt,
+                  logit_dt=w.logit_dt, q=take(w.q), k=take(w.k), v=take(w.v),
+                  k_scale=None if w.k_scale is None else w.k_scale.cpu().numpy(),
+                  v_scale=None if w.v_scale is None else w.v_scale.cpu().numpy(),
+                  kv_len=w.kv_len[r], parent=w.parent[r], tokens=w.tokens[r],
+                  target_logits=take(w.target_logits) if with_logits else None, draft_logits=None,
+                  uniforms=None if w.uniforms is None else w.uniforms[r], temperature=w.temperature,
+                  name=w.name, meta=dict(w.meta, requests=[int(x) for x in r]))
 
 
 # ----------------------------------------------------------------------------------------------------
@@ -492,10 +611,13 @@ WORKLOADS = {
 }
 
 
-def make_workload(name: str, seed: int = 0, **overrides):
+def make_workload(name: str, seed: int = 0, device=None, **overrides):
+    """A named workload; device="cuda" draws a verify batch with make_verify_device (greedy / one-hot)."""
     cfg = dict(WORKLOADS[name])
     cfg.update(overrides)
     kind = cfg.pop("kind")
     if kind == "loss":
         return make_loss(seed, name=name, **cfg)
+    if device is not None:
+        return make_verify_device(seed, name=name, device=device, **cfg)
     return make_verify(seed, name=name, **cfg)

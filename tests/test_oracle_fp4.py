@@ -72,3 +72,19 @@ def test_fp4_statuses():
     kv_len[1] = w.kv_cap
     out, lse, st, rc = oracle.tree_attn_e2m1(w.q, kp, vp, kb, vb, ks, vs, kv_len, parent, Hq=w.Hq, q_dt="f32")
     assert list(st) == [2, 1, 0]
+
+
+def test_fp4_sampled_rows_equal_the_full_computation():
+    # the sampled-row form (used by the full-size GPU parity tests) computes exactly the listed rows
+    w, (kp, vp, kb, vb, ks, vs) = batch(5, (3, 2, 2), 13)
+    full, full_lse, _, _ = oracle.tree_attn_e2m1(w.q, kp, vp, kb, vb, ks, vs, w.kv_len, w.parent, Hq=w.Hq, q_dt="f32")
+    rows = np.array([[2, 12, 3], [0, 0, 0], [2, 5, 1], [1, 7, 2]], np.int32)
+    out, lse, st, rc = oracle.tree_attn_e2m1(w.q, kp, vp, kb, vb, ks, vs, w.kv_len, w.parent, Hq=w.Hq, q_dt="f32",
+                                             rows=rows)
+    assert rc == 0
+    b, i, h = rows.T
+    np.testing.assert_array_equal(out[b, i, h], full[b, i, h])
+    np.testing.assert_array_equal(lse[b, i, h], full_lse[b, i, h])
+    mask = np.ones(lse.shape, bool)
+    mask[b, i, h] = False
+    assert np.isnan(lse[mask]).all()

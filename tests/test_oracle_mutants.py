@@ -59,7 +59,8 @@ MUTANTS = {
         "dv[row * D + d] += p * g[d];", "dv[row * D + d] += p * qv[d];",
         TB.test_backward_matches_central_finite_differences),
     "fp4_high_nibble_first": (
-        "unsigned kc = (k[i / 2] >> (4 * (i & 1))) & 15,", "unsigned kc = (k[i / 2] >> (4 * (1 - (i & 1)))) & 15,",
+        "unsigned kc = (k[(base + i) / 2] >> (4 * (i & 1))) & 15,",
+        "unsigned kc = (k[(base + i) / 2] >> (4 * (1 - (i & 1)))) & 15,",
         lambda: TF.test_fp4_attention_equals_attention_on_independently_decoded_caches((3, 2, 2), 13)),
     "fx_poly_drops_cubic": (
         "p = fmaf(p, f, C_P3);", "p = fmaf(p, f, 0.0f);", TA.test_fx_exp2_polynomial_error_bound),
