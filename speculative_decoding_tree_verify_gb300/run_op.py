@@ -1,10 +1,11 @@
 """Run one library call repeatedly on a named synthetic workload (for profilers such as ncu).
 
 python -m speculative_decoding_tree_verify_gb300.run_op --op OP --workload NAME [--reps N]
-                                                        [--batch B] [--mode greedy|onehot|prob]
+                                                        [--batch B] [--mode greedy|onehot|prob] [--device-recipe]
 OP: attn, accept, loss, attn_bwd (forward once, then the backward), attn_paged (caches in 128-row pages),
 compact (random accepted root paths), expand (the widest level of the workload's tree).
-Inputs are generated once and stay on the device; the call is repeated --reps times.
+Inputs are generated once and stay on the device; the call is repeated --reps times.  --device-recipe draws
+a greedy / one-hot verify batch on the GPU (the generator's device recipe), for full-size batches.
 """
 from __future__ import annotations
 
@@ -20,6 +21,8 @@ from . import workloads as W
 def _dev(a):
     if a is None:
         return None
+    if isinstance(a, torch.Tensor):
+        return a.cuda()
     a = np.ascontiguousarray(a)
     if a.dtype == np.uint16:
         a = a.view(np.int16)
@@ -38,6 +41,7 @@ def main():
     ap.add_argument("--mode", default=None, help="override the acceptance mode")
     ap.add_argument("--temperature", type=float, default=None)
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--device-recipe", action="store_true", help="draw the verify batch on the GPU")
     args = ap.parse_args()
     over = {}
     if args.batch is not None:
@@ -48,6 +52,9 @@ def main():
         over["temperature"] = args.temperature
     if args.op in ("accept", "expand"):
         over["with_attn"] = False
+    if args.device_recipe:
+        over.pop("with_attn", None)
+        over["device"] = "cuda"
     w = W.make_workload(args.workload, seed=args.seed, **over)
     i32 = dict(dtype=torch.int32, device="cuda")
     if args.op == "attn":

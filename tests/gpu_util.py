@@ -6,9 +6,12 @@ from speculative_decoding_tree_verify_gb300 import sv
 
 
 def dev(a):
-    """numpy array from the generators -> CUDA tensor with the same bytes (bf16 bits travel as int16)."""
+    """numpy array from the generators -> CUDA tensor with the same bytes (bf16 bits travel as int16); tensors
+    drawn on the GPU by the generator's device recipe pass through."""
     if a is None:
         return None
+    if isinstance(a, torch.Tensor):
+        return a.cuda()
     a = np.ascontiguousarray(a)
     if a.dtype == np.uint16:
         a = a.view(np.int16)

@@ -131,6 +131,27 @@ def test_attn_fp8_tensor_core_parity(case):
 
 
 def test_fp8_long_context_attention_sampled():
-    # config-5 requests (T=64, 64/8 heads, e4m3 KV, L in [8192, 32768]) at 16 requests, the most whose caches
-    # the host generator can build for the oracle in a test
+    # config-5 requests (T=64, 64/8 heads, e4m3 KV, L in [8192, 32768]) at 16 requests drawn on the host
     check_sampled(W.make_workload("fp8_long_context", seed=0, B=16))
+
+
+def test_fp8_long_context_full_batch_sampled_rows():
+    # the whole 128-request batch in the launch configuration the bench times (drawn on the GPU by the generator's
+    # device recipe); the oracle recomputes sampled rows of 12 requests, the first and last included, and every
+    # node of one of them at 8 heads
+    w = W.make_workload("fp8_long_context", seed=0, device="cuda")
+    out, lse, st = run_attn(w)
+    assert (st == 0).all()
+    rng = np.random.default_rng(7)
+    reqs = sorted({0, w.B - 1, *[int(x) for x in rng.choice(w.B, 10, replace=False)]})
+    h = W.host_requests(w, reqs, with_logits=False)
+    rows = [[j, int(rng.integers(0, w.T)), int(rng.integers(0, w.Hq))] for j in range(len(reqs)) for _ in range(24)]
+    rows += [[1, i, hh] for i in range(w.T) for hh in range(0, w.Hq, 8)]
+    rows = np.array(rows, np.int32)
+    ref_o, ref_l, ref_st, _ = oracle.tree_attn_w(h, rows=rows)
+    assert (ref_st == 0).all()
+    j, i, hh = rows.T
+    b = np.asarray(reqs)[j]
+    err = np.abs(out[b, i, hh] - ref_o[j, i, hh]).max()
+    assert err <= 6e-2, err
+    assert np.abs(lse[b, i, hh] - ref_l[j, i, hh]).max() <= 1e-3

@@ -7,11 +7,14 @@ file runs last so that a stop-at-first-failure run has already run every other t
 fresh process as well as after the rest.
 
 Each case makes two sv_accept_noalloc calls in a row on different inputs (the second finds the first's
-leftovers in the shared array) and compares every integer output of both with sv_accept's, bit for bit.
+leftovers in the shared array) and compares every integer output of both with sv_accept's, bit for bit, and
+the first call's with the CPU oracle's as well.  One case uses the scratch to its last row.
 """
 import numpy as np
 import pytest
 import torch
+
+import oracle
 
 from speculative_decoding_tree_verify_gb300 import sv
 from speculative_decoding_tree_verify_gb300 import workloads as W
@@ -51,7 +54,7 @@ CASES = [
 
 @pytest.mark.parametrize("name,first,second", CASES, ids=[c[0] for c in CASES])
 def test_noalloc_matches_accept_two_calls(name, first, second):
-    for over in (first, second):
+    for n, over in enumerate((first, second)):
         over = dict(over)
         seed = over.pop("seed")
         w = W.make_workload(name, seed=seed, with_attn=False, **over)
@@ -60,6 +63,28 @@ def test_noalloc_matches_accept_two_calls(name, first, second):
         for k in KEYS:
             np.testing.assert_array_equal(got[k], want[k], err_msg=k)
         assert (got["status"] == 0).all()
+        if n == 0:
+            ref = oracle.accept_w(w)
+            for k in KEYS:
+                np.testing.assert_array_equal(got[k], ref[k], err_msg=f"oracle {k}")
+
+
+def test_noalloc_uses_the_whole_scratch():
+    # 16384 chains of 4 nodes = 65536 target rows, the scratch's limit, with draft rows (stochastic, PROB mode):
+    # the array's last row records are written and read; then a small call reuses the array
+    w = W.make_verify(11, B=16384, T=4, Hq=1, Hkv=1, D=16, L=(0, 0), V=16, q_dt="f32", kv_dt="f32",
+                      logit_dt="bf16", tree="chain", mode="prob", temperature=0.9, with_attn=False)
+    for case in (w, W.make_verify(12, B=3, T=4, Hq=1, Hkv=1, D=16, L=(0, 0), V=16, logit_dt="bf16", tree="chain",
+                                  mode="prob", temperature=0.9, with_attn=False)):
+        want = _call(sv.accept, case, case.temperature)
+        got = _call(sv.accept_noalloc, case, case.temperature)
+        for k in KEYS:
+            np.testing.assert_array_equal(got[k], want[k], err_msg=k)
+        assert (got["status"] == 0).all()
+    ref = oracle.accept_w(w)
+    got = _call(sv.accept_noalloc, w, w.temperature)
+    for k in KEYS:
+        np.testing.assert_array_equal(got[k], ref[k], err_msg=f"oracle {k}")
 
 
 def test_noalloc_rejects_oversized_batch():
