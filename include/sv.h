@@ -55,7 +55,8 @@ typedef enum {
     SV_ERR_WORKSPACE = 8         /* workspace NULL or smaller than sv_workspace_size()                   */
 } sv_status;
 
-typedef enum { SV_F32 = 0, SV_BF16 = 1, SV_E4M3 = 2 } sv_dtype;
+/* SV_E2M1: FP4 caches in the NVFP4 layout, only through sv_tree_attn_fp4 (codes plus block scales). */
+typedef enum { SV_F32 = 0, SV_BF16 = 1, SV_E4M3 = 2, SV_E2M1 = 3 } sv_dtype;
 
 typedef enum { SV_OP_TREE_ATTN = 0, SV_OP_ACCEPT = 1, SV_OP_LOSS = 2, SV_OP_TREE_ATTN_BWD = 3 } sv_op;
 
@@ -104,6 +105,31 @@ sv_status sv_tree_attn(int B, int T, int Hq, int Hkv, int D, int kv_cap, sv_dtyp
                        sv_stream_t stream);
 
 /*
+ * sv_tree_attn_fp4 -- sv_tree_attn over FP4 KV caches.
+ *
+ * The pages name FP4 among the serving stack's precisions ("Aurora" post, section 1: production speed-up depends
+ * on the kernels and their numerical precision, FP8/FP4) but fix no format.  This call reads the NVFP4 layout the
+ * GB300 tensor cores use natively: OCP E2M1 codes, two per byte with the even element in the low nibble, one
+ * E4M3 block scale per 16 consecutive elements of a cache row, and an fp32 scale per kv head:
+ *     K[b, hk, j, d] = e2m1(code) * e4m3(k_block[b, hk, j, d / 16]) * k_scale[hk]      (V likewise)
+ * The attention is exactly sv_tree_attn's ("Aurora" post, section 2) over those values.
+ *   k_codes, v_codes   uint8 [B, Hkv, kv_cap, D/2]
+ *   k_block, v_block   uint8 [B, Hkv, kv_cap, D/16] E4M3 codes
+ *   k_scale, v_scale   float [Hkv]
+ *   q, kv_len, parent, sm_scale, out, lse, status, workspace: as for sv_tree_attn
+ * Shapes: q_dt SV_BF16, D = 128, kv_cap even, 1 <= T <= 64, Hq % Hkv == 0; all cache pointers 16-byte aligned.
+ * Tensor cores: every decoded value (a 2-bit-mantissa code times a 4-bit-mantissa scale) is exactly an f16 value,
+ * so the caches are expanded to f16 in shared memory and the MMAs run on f16 operands (Q rounded to f16), with
+ * fp32 accumulation; the head scales fold into the softmax scale and the output.  Workspace: as sv_tree_attn's
+ * (sv_workspace_size(SV_OP_TREE_ATTN, ...)).  Anything else returns SV_ERR_UNSUPPORTED.
+ */
+sv_status sv_tree_attn_fp4(int B, int T, int Hq, int Hkv, int D, int kv_cap, sv_dtype q_dt, const void* q,
+                           const void* k_codes, const void* v_codes, const void* k_block, const void* v_block,
+                           const float* k_scale, const float* v_scale, const int32_t* kv_len, const int32_t* parent,
+                           float sm_scale, void* out, float* lse, int32_t* status, void* workspace, size_t ws_bytes,
+                           sv_stream_t stream);
+
+/*
  * sv_tree_attn_paged -- sv_tree_attn over a paged KV cache.
  *
  * Serving systems keep the KV cache in fixed-size pages shared by all requests and give each request a
@@ -115,15 +141,18 @@ sv_status sv_tree_attn(int B, int T, int Hq, int Hkv, int D, int kv_cap, sv_dtyp
  *   page_table      int32 [B, max_pages]; entries past the pages a request reads are ignored
  *   page_size       a power of two
  *   q, out, lse, kv_len, parent, sm_scale, status: as for sv_tree_attn, with kv_cap = max_pages * page_size
+ *   workspace / ws_bytes: at least sv_workspace_size(SV_OP_TREE_ATTN, B, T, Hq, Hkv, D, max_pages * page_size, 0)
+ *                   bytes, 256-byte aligned, when that size is not 0 (else may be NULL)
  * A request whose kv_len + T exceeds max_pages * page_size, or that reads a page id outside
- * [0, num_pages), gets status SV_ERR_INVALID_ARG and zero outputs.  Runs on the CUDA-core attention kernel
- * (fp32 arithmetic, any D up to 256); no workspace.
+ * [0, num_pages), gets status SV_ERR_INVALID_ARG and zero outputs.  bf16 Q with bf16 or e4m3 pools, D = 128 and
+ * pages of at least 8 rows run on the tensor-core kernel (the K/V tiles are gathered page by page by TMA);
+ * everything else on the CUDA-core attention kernel (fp32 arithmetic, any D up to 256).
  */
 sv_status sv_tree_attn_paged(int B, int T, int Hq, int Hkv, int D, int page_size, int max_pages, int num_pages,
                              sv_dtype q_dt, sv_dtype kv_dt, const void* q, const void* k_pool, const void* v_pool,
                              const float* k_scale, const float* v_scale, const int32_t* page_table,
                              const int32_t* kv_len, const int32_t* parent, float sm_scale, void* out, float* lse,
-                             int32_t* status, sv_stream_t stream);
+                             int32_t* status, void* workspace, size_t ws_bytes, sv_stream_t stream);
 
 /*
  * sv_accept -- verify one batch of draft trees against the target's per-node logits.

@@ -72,11 +72,37 @@ sv_status sv_tree_attn(int B, int T, int Hq, int Hkv, int D, int kv_cap, sv_dtyp
     return from_cuda(tc ? launch_attn_tc(a, s) : launch_attn_simt(a, s));
 }
 
+sv_status sv_tree_attn_fp4(int B, int T, int Hq, int Hkv, int D, int kv_cap, sv_dtype q_dt, const void* q,
+                           const void* k_codes, const void* v_codes, const void* k_block, const void* v_block,
+                           const float* k_scale, const float* v_scale, const int32_t* kv_len, const int32_t* parent,
+                           float sm_scale, void* out, float* lse, int32_t* status, void* workspace, size_t ws_bytes,
+                           sv_stream_t stream) {
+    if (T > SV_MAX_T) return SV_ERR_TREE_TOO_LARGE;
+    if (B < 0 || B > 65535 || T < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || D < 1 || kv_cap < T) return SV_ERR_INVALID_ARG;
+    if (!(sm_scale >= 0.f) || isinf(sm_scale)) return SV_ERR_INVALID_ARG;
+    if (q_dt != SV_BF16 || D != 128 || kv_cap % 2) return SV_ERR_UNSUPPORTED;
+    if (B == 0) return SV_OK;
+    if (!q || !k_codes || !v_codes || !k_block || !v_block || !k_scale || !v_scale || !kv_len || !parent || !out)
+        return SV_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_codes, 16) || !aligned(v_codes, 16) || !aligned(k_block, 16) ||
+        !aligned(v_block, 16) || !aligned(out, 16) || !aligned(kv_len, 4) || !aligned(parent, 4) || !aligned(lse, 4) ||
+        !aligned(status, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4))
+        return SV_ERR_UNSUPPORTED;
+    AttnArgs a{B, T, Hq, Hkv, D, kv_cap, q_dt, SV_E2M1, q, k_codes, v_codes, k_scale, v_scale, kv_len, parent,
+               sm_scale, out, lse, status, workspace, ws_bytes};
+    a.k_block = k_block;
+    a.v_block = v_block;
+    if (!attn_tc_supported(a)) return SV_ERR_UNSUPPORTED;
+    const size_t need = attn_workspace_size(B, T, Hq, Hkv, D, kv_cap);
+    if (!workspace || ws_bytes < need || !aligned(workspace, 256)) return SV_ERR_WORKSPACE;
+    return from_cuda(launch_attn_tc(a, (cudaStream_t)stream));
+}
+
 sv_status sv_tree_attn_paged(int B, int T, int Hq, int Hkv, int D, int page_size, int max_pages, int num_pages,
                              sv_dtype q_dt, sv_dtype kv_dt, const void* q, const void* k_pool, const void* v_pool,
                              const float* k_scale, const float* v_scale, const int32_t* page_table,
                              const int32_t* kv_len, const int32_t* parent, float sm_scale, void* out, float* lse,
-                             int32_t* status, sv_stream_t stream) {
+                             int32_t* status, void* workspace, size_t ws_bytes, sv_stream_t stream) {
     if (T > SV_MAX_T) return SV_ERR_TREE_TOO_LARGE;
     if (B < 0 || B > 65535 || T < 1 || Hq < 1 || Hkv < 1 || Hkv > 65535 || Hq % Hkv || D < 1) return SV_ERR_INVALID_ARG;
     if (page_size < 1 || (page_size & (page_size - 1)) || max_pages < 1 || num_pages < 1) return SV_ERR_INVALID_ARG;
@@ -95,12 +121,20 @@ sv_status sv_tree_attn_paged(int B, int T, int Hq, int Hkv, int D, int page_size
     int shift = 0;
     while ((1 << shift) < page_size) ++shift;
     AttnArgs a{B, T, Hq, Hkv, D, page_size * max_pages, q_dt, kv_dt, q, k_pool, v_pool, k_scale, v_scale, kv_len,
-               parent, sm_scale, out, lse, status, nullptr, 0};
+               parent, sm_scale, out, lse, status, workspace, ws_bytes};
     a.page_table = page_table;
     a.page_shift = shift;
     a.max_pages = max_pages;
     a.num_pages = num_pages;
-    return from_cuda(launch_attn_simt(a, (cudaStream_t)stream));
+    // the tensor-core kernel reads whole 16-byte-aligned rows through TMA
+    const bool tc = attn_tc_supported(a) && aligned(q, 16) && aligned(k_pool, 16) && aligned(v_pool, 16) &&
+                    aligned(out, 16);
+    if (tc) {
+        const size_t need = attn_workspace_size(B, T, Hq, Hkv, D, page_size * max_pages);
+        if (!workspace || ws_bytes < need || !aligned(workspace, 256)) return SV_ERR_WORKSPACE;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    return from_cuda(tc ? launch_attn_tc(a, s) : launch_attn_simt(a, s));
 }
 
 sv_status sv_accept(int B, int T, int V, sv_dtype logit_dt, const void* target_logits,

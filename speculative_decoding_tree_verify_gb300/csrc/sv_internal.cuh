@@ -75,8 +75,11 @@ struct AttnArgs {
     int32_t* status;
     void* ws;
     size_t ws_bytes;
-    // paged caches (CUDA-core path only): k / v are pools [num_pages, Hkv, page_size, D]; logical position j
-    // of request b lives in page page_table[b * max_pages + j / page_size] at offset j % page_size
+    // FP4 (e2m1) caches: k / v hold the codes [B, Hkv, kv_cap, D/2]; these the e4m3 block scales [.., D/16]
+    const void* k_block = nullptr;
+    const void* v_block = nullptr;
+    // paged caches: k / v are pools [num_pages, Hkv, page_size, D]; logical position j of request b lives in page
+    // page_table[b * max_pages + j / page_size] at offset j % page_size
     const int32_t* page_table = nullptr;
     int page_shift = 0;   // log2(page_size)
     int max_pages = 0;

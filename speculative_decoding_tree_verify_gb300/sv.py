@@ -16,7 +16,7 @@ LIB_PATH = Path(__file__).resolve().parent / "_build" / "libsv.so"
 
 OK, ERR_INVALID_ARG, ERR_BAD_TREE, ERR_TREE_TOO_LARGE, ERR_UNSUPPORTED, ERR_NONFINITE, ERR_TIMEOUT, ERR_CUDA, \
     ERR_WORKSPACE = range(9)
-F32, BF16, E4M3 = 0, 1, 2
+F32, BF16, E4M3, E2M1 = 0, 1, 2, 3
 OP_TREE_ATTN, OP_ACCEPT, OP_LOSS, OP_TREE_ATTN_BWD = 0, 1, 2, 3
 
 _lib = None
@@ -49,8 +49,10 @@ def lib() -> C.CDLL:
         L.sv_loss.restype = i
         L.sv_accept_noalloc.argtypes = [i, i, i, i, P, P, P, P, f, P, P, P, P, P, P, P, P]
         L.sv_accept_noalloc.restype = i
-        L.sv_tree_attn_paged.argtypes = [i, i, i, i, i, i, i, i, i, i, P, P, P, P, P, P, P, P, f, P, P, P, P]
+        L.sv_tree_attn_paged.argtypes = [i, i, i, i, i, i, i, i, i, i, P, P, P, P, P, P, P, P, f, P, P, P, P, z, P]
         L.sv_tree_attn_paged.restype = i
+        L.sv_tree_attn_fp4.argtypes = [i, i, i, i, i, i, i, P, P, P, P, P, P, P, P, P, f, P, P, P, P, z, P]
+        L.sv_tree_attn_fp4.restype = i
         L.sv_tree_attn_bwd.argtypes = [i, i, i, i, i, i, i, i, P, P, P, P, P, f, P, P, P, P, P, P, P, P, z, P]
         L.sv_tree_attn_bwd.restype = i
         L.sv_kv_compact.argtypes = [i, i, i, i, i, i, P, P, P, P, P, P, P, P, P]
@@ -121,16 +123,32 @@ def tree_attn(q, k_cache, v_cache, kv_len, parent, out, *, k_scale=None, v_scale
 
 
 def tree_attn_paged(q, k_pool, v_pool, page_table, kv_len, parent, out, *, k_scale=None, v_scale=None, sm_scale=0.0,
-                    lse=None, status=None, stream=None):
+                    lse=None, status=None, workspace=None, stream=None):
     """sv_tree_attn_paged: q [B,T,Hq,D]; pools [num_pages,Hkv,page_size,D]; page_table [B,max_pages]; out like q."""
     B, T, Hq, D = q.shape
     num_pages, Hkv, page_size = k_pool.shape[0], k_pool.shape[1], k_pool.shape[2]
     max_pages = page_table.shape[1]
+    ws = _ws(OP_TREE_ATTN, workspace, B, T, Hq, Hkv, D, page_size * max_pages, 0)
     code = lib().sv_tree_attn_paged(B, T, Hq, Hkv, D, page_size, max_pages, num_pages, dtype_code(q),
                                     dtype_code(k_pool), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
                                     _ptr(v_scale), _ptr(page_table), _ptr(kv_len), _ptr(parent), float(sm_scale),
-                                    _ptr(out), _ptr(lse), _ptr(status), _stream(stream))
+                                    _ptr(out), _ptr(lse), _ptr(status), _ptr(ws),
+                                    0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
     _check(code, "sv_tree_attn_paged")
+
+
+def tree_attn_fp4(q, k_codes, v_codes, k_block, v_block, k_scale, v_scale, kv_len, parent, out, *, sm_scale=0.0,
+                  lse=None, status=None, workspace=None, stream=None):
+    """sv_tree_attn_fp4: q [B,T,Hq,D] bf16; codes [B,Hkv,kv_cap,D/2] uint8; block scales [B,Hkv,kv_cap,D/16] uint8
+    (E4M3); head scales [Hkv] float; out like q."""
+    B, T, Hq, D = q.shape
+    Hkv, kv_cap = k_codes.shape[1], k_codes.shape[2]
+    ws = _ws(OP_TREE_ATTN, workspace, B, T, Hq, Hkv, D, kv_cap, 0)
+    code = lib().sv_tree_attn_fp4(B, T, Hq, Hkv, D, kv_cap, dtype_code(q), _ptr(q), _ptr(k_codes), _ptr(v_codes),
+                                  _ptr(k_block), _ptr(v_block), _ptr(k_scale), _ptr(v_scale), _ptr(kv_len),
+                                  _ptr(parent), float(sm_scale), _ptr(out), _ptr(lse), _ptr(status), _ptr(ws),
+                                  0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
+    _check(code, "sv_tree_attn_fp4")
 
 
 def accept(target_logits, tokens, parent, accept_len, path, out_tokens, bonus, *, draft_logits=None,

@@ -124,11 +124,12 @@ def test_loss_host_validation(L):
 
 def paged(L, **kw):
     a = dict(B=2, T=4, Hq=4, Hkv=2, D=64, P=16, maxp=8, nump=20, q_dt=sv.BF16, kv_dt=sv.BF16, q=FAKE, k=FAKE, v=FAKE,
-             ks=None, vs=None, pt=FAKE, kv_len=FAKE, parent=FAKE, scale=0.0, out=FAKE, lse=None, st=None)
+             ks=None, vs=None, pt=FAKE, kv_len=FAKE, parent=FAKE, scale=0.0, out=FAKE, lse=None, st=None, ws=None,
+             ws_bytes=0)
     a.update(kw)
     return L.sv_tree_attn_paged(a["B"], a["T"], a["Hq"], a["Hkv"], a["D"], a["P"], a["maxp"], a["nump"], a["q_dt"],
                                 a["kv_dt"], a["q"], a["k"], a["v"], a["ks"], a["vs"], a["pt"], a["kv_len"], a["parent"],
-                                a["scale"], a["out"], a["lse"], a["st"], None)
+                                a["scale"], a["out"], a["lse"], a["st"], a["ws"], a["ws_bytes"], None)
 
 
 def test_tree_attn_paged_host_validation(L):
@@ -145,6 +146,28 @@ def test_tree_attn_paged_host_validation(L):
     assert paged(L, kv_dt=sv.E4M3) == sv.ERR_INVALID_ARG       # e4m3 needs its scales
     assert paged(L, k=ODD) == sv.ERR_UNSUPPORTED
     assert paged(L, B=0) == sv.OK
+
+
+def attn_fp4(L, **kw):
+    a = dict(B=2, T=4, Hq=4, Hkv=2, D=128, kv_cap=64, q_dt=sv.BF16, q=FAKE, kc=FAKE, vc=FAKE, kb=FAKE, vb=FAKE,
+             ks=FAKE, vs=FAKE, kv_len=FAKE, parent=FAKE, scale=0.0, out=FAKE, lse=None, st=None, ws=None, ws_bytes=0)
+    a.update(kw)
+    return L.sv_tree_attn_fp4(a["B"], a["T"], a["Hq"], a["Hkv"], a["D"], a["kv_cap"], a["q_dt"], a["q"], a["kc"], a["vc"],
+                              a["kb"], a["vb"], a["ks"], a["vs"], a["kv_len"], a["parent"], a["scale"], a["out"],
+                              a["lse"], a["st"], a["ws"], a["ws_bytes"], None)
+
+
+def test_tree_attn_fp4_host_validation(L):
+    assert attn_fp4(L, T=65) == sv.ERR_TREE_TOO_LARGE
+    assert attn_fp4(L, Hq=3) == sv.ERR_INVALID_ARG
+    assert attn_fp4(L, kv_cap=2) == sv.ERR_INVALID_ARG          # capacity below T
+    assert attn_fp4(L, D=64) == sv.ERR_UNSUPPORTED
+    assert attn_fp4(L, q_dt=sv.F32) == sv.ERR_UNSUPPORTED
+    assert attn_fp4(L, kv_cap=65) == sv.ERR_UNSUPPORTED         # odd capacity: block scales read two rows at a time
+    assert attn_fp4(L, kb=None) == sv.ERR_INVALID_ARG
+    assert attn_fp4(L, vs=None) == sv.ERR_INVALID_ARG
+    assert attn_fp4(L, kc=ODD) == sv.ERR_UNSUPPORTED
+    assert attn_fp4(L, B=0) == sv.OK
 
 
 def attn_bwd(L, **kw):

@@ -115,6 +115,8 @@ FP8_TC = [
     (3, 13, 16, 2, (1, 700), (3, 2, 2)),
     (2, 60, 32, 8, (2048, 3000), (4, 3, 2, 2, 1, 1)),
     (2, 64, 64, 8, (8192, 9000), (4, 3, 2, 2, 1, 1, 1)),
+    (2, 11, 9, 3, (90, 400), (3, 2, 2)),        # G = 3: the softmax warps write Q (rounded to f16)
+    (2, 20, 32, 2, (64, 300), (4, 2, 2)),       # 320 rows per kv head: one pair unit and one split unit
 ]
 
 
