@@ -60,6 +60,8 @@ def parse(argv=None):
     ap.add_argument("--ops", nargs="*", default=None,
                     help="instead of the step: time every library call on the named workloads (all if none given), "
                          "one JSON line per call")
+    ap.add_argument("--calls", default="attn,accept,loss,bwd,paged,compact,expand",
+                    help="with --ops: the calls to time (comma-separated)")
     return ap.parse_args(argv)
 
 
@@ -657,7 +659,7 @@ def run_ops(args):
         kl, par = dev(w.kv_len), dev(w.parent)
         fn = lambda: sv.tree_attn(q, k, v, kl, par, out, k_scale=ks, v_scale=vs, lse=lse, status=st, workspace=ws)
         us = timed(fn, reps=5 if w.kv_dt == "e4m3" else 10)
-        assert (st == 0).all()
+        assert (st == 0).all(), f"tree_attn statuses {st.cpu().tolist()}"
         report(name, "tree_attn", us, attn_bytes(w), "tensor cores" if tensor_core_attn(w) else "CUDA cores",
                flops=attn_flops(w))
 
@@ -759,25 +761,33 @@ def run_ops(args):
             report(name, f"tree_expand_level{dd + 1}", us, nb, f"{nf} x top-{kk} -> {nk}")
         report(name, "tree_expand_all_levels", tot_us, tot_b, f"{len(levels)} calls")
 
+    calls = set(args.calls.split(","))
     which = args.ops or ["tiny_chain", "llama3_8b_tree", "qwen3_8b_stochastic", "loss_batch", "fp8_long_context"]
     for name in which:
         if name == "loss_batch":
-            loss_case(name, W.make_workload(name, seed=args.seed))
+            if "loss" in calls:
+                loss_case(name, W.make_workload(name, seed=args.seed))
             continue
         w = load_workload(name, args.seed)
-        attn_case(name, w)
-        for label, temp, with_draft in accept_modes(w):
-            accept_case(name, w, temp, w.draft_logits if with_draft else None)
+        if "attn" in calls:
+            attn_case(name, w)
+        if "accept" in calls:
+            for label, temp, with_draft in accept_modes(w):
+                accept_case(name, w, temp, w.draft_logits if with_draft else None)
         if name in ("llama3_8b_tree", "qwen3_8b_stochastic"):
-            bwd_case(name, w)
-            paged_case(name, w)
-        compact_case(name, w.B, w.T, w.Hkv, w.D, w.kv_cap, w.kv_dt, w.kv_len, w.parent, args.seed)
-        if name == "llama3_8b_tree":
-            expand_case(name, w.B, w.V, W.expansion_levels(60, (4, 3, 2, 2, 1, 1)), 3.0, 200 + args.seed)
-        elif name == "qwen3_8b_stochastic":
-            expand_case(name, w.B, w.V, [(1, 1, 1)] * 5, 2.5, 300 + args.seed)
-        elif name == "fp8_long_context":
-            expand_case(name, w.B, w.V, W.expansion_levels(64, (4, 3, 2, 2, 1, 1, 1)), 3.0, 500 + args.seed)
+            if "bwd" in calls:
+                bwd_case(name, w)
+            if "paged" in calls:
+                paged_case(name, w)
+        if "compact" in calls:
+            compact_case(name, w.B, w.T, w.Hkv, w.D, w.kv_cap, w.kv_dt, w.kv_len, w.parent, args.seed)
+        if "expand" in calls:
+            if name == "llama3_8b_tree":
+                expand_case(name, w.B, w.V, W.expansion_levels(60, (4, 3, 2, 2, 1, 1)), 3.0, 200 + args.seed)
+            elif name == "qwen3_8b_stochastic":
+                expand_case(name, w.B, w.V, [(1, 1, 1)] * 5, 2.5, 300 + args.seed)
+            elif name == "fp8_long_context":
+                expand_case(name, w.B, w.V, W.expansion_levels(64, (4, 3, 2, 2, 1, 1, 1)), 3.0, 500 + args.seed)
         del w
         torch.cuda.empty_cache()
 

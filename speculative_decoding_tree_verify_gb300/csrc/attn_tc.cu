@@ -25,6 +25,8 @@
 //   warp 0       K producer: the segment's Q (TMA 3D boxes) and the K tiles into a 2-slot K ring
 //   warp 1       MMA issuer (also owns the 512 TMEM columns): S_A, S_B, O_A += P_A V, O_B += P_B V in the
 //                order that lets one side's MMAs overlap the other side's softmax
+//   warp 2       (bf16 caches) V cleaner: passes every V tile to the MMAs, zeroing the cache rows past the tree
+//                block in a unit's last tile
 //   warp 3       V producer: the V tiles into a 2-slot V ring
 //   warps 4-7    softmax of side A, warps 8-11 softmax of side B: one thread per query row (TMEM lane), all
 //                128 scores of the row in registers; the row max needs no exchange between threads
@@ -335,13 +337,23 @@ struct TileRows {
 };
 
 // ------------------------------------------------------------------------------------------------ main kernel
+// A softmax warp's segment walk and the segment whose epilogue is pending (written by lane 0, read by all lanes).
+struct SoftmaxState {
+    SegIter it;
+    Seg seg, pend;
+    uint32_t pend_nseg;
+    int pend_on, has;
+};
+
 struct MainShared {
     uint64_t full[4], raw[4], empty[4];                    // K slots 0, 1 and V slots 2, 3
     uint64_t s_full[2], p_full[2], o_full[2];              // per side
     uint64_t o_free;                                       // the segment's O has been read by both sides
     uint64_t q_full, q_ready, q_empty, drain[2];
     uint64_t conv_bar;                                     // e2m1 caches: the converters have read the raw tile
-    float ml[2][2][kRows];                                 // split-mode epilogue: [side][m, l][row]
+    float ml[2][2][kRows];                                 // split-mode epilogue: [side][m][row]
+    float pm[2][kRows], pl[2][kRows];                      // pending epilogue: the row's max and sum, per side
+    SoftmaxState sm[8];                                    // per softmax warp: segment walk and pending epilogue
     Plan plan;
     long long scan[33];
     int32_t par[SV_MAX_T];                                 // parent array of the current request
@@ -356,7 +368,8 @@ template <int KVK>
 __global__ void __launch_bounds__(threads_of<KVK>(), 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKs,
-               const __grid_constant__ CUtensorMap tmVs, AttnArgs a, float scale_log2, int q_tma, int box_rows) {
+               const __grid_constant__ CUtensorMap tmVs, const __grid_constant__ AttnArgs a, float scale_log2, int q_tma,
+               int box_rows) {
     constexpr bool CONV = KVK != KV_BF16;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -369,8 +382,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 
     if (tid == 0) {
         for (int i = 0; i < 4; ++i) {
-            mbar_init(&sh.full[i], CONV ? 4 : 1);    // the TMA transaction, or one arrival per converter warp
-            mbar_init(&sh.raw[i], 1);
+            // K (bf16): the TMA transaction; V (bf16): the V cleaner; 8-bit / 4-bit: one arrival per converter warp
+            mbar_init(&sh.full[i], CONV ? 4 : 1);
+            mbar_init(&sh.raw[i], 1);                // the raw tile's TMA transaction
             mbar_init(&sh.empty[i], 1);              // the MMA warp's commit after the tile's last reader
         }
         for (int s = 0; s < 2; ++s) {
@@ -438,11 +452,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                     if (!mbar_wait(&sh.empty[gslot], (round & 1) ^ 1, err)) break;
                     uint8_t* dst = smem + (kv ? kSmemV : kSmemK) + slot * kSlotBytes;
                     if constexpr (KVK == KV_BF16) {
-                        mbar_arrive_expect_tx(&sh.full[gslot], kSlotBytes);
+                        // K tiles go straight to the MMAs; V tiles pass the V cleaner first
+                        uint64_t* bar = kv ? &sh.raw[gslot] : &sh.full[gslot];
+                        mbar_arrive_expect_tx(bar, kSlotBytes);
                         for (int bx = 0; bx < nbox; ++bx) {
                             const int y = tr.y(sg.b, sg.hk, L, t, bx);
-                            tma_load_2d(dst + bx * box_rows * 128, tm, 0, y, &sh.full[gslot]);
-                            tma_load_2d(dst + kBoxBytes + bx * box_rows * 128, tm, 64, y, &sh.full[gslot]);
+                            tma_load_2d(dst + bx * box_rows * 128, tm, 0, y, bar);
+                            tma_load_2d(dst + kBoxBytes + bx * box_rows * 128, tm, 64, y, bar);
                         }
                     } else if constexpr (KVK == KV_E4M3) {
                         mbar_arrive_expect_tx(&sh.raw[gslot], kBoxBytes);
@@ -548,6 +564,38 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             mbar_wait(&sh.drain[0], 0, &local);
         }
         __syncwarp();
+    } else if (warp == 2) {
+        // ---------------------------------------------------------------- V cleaner (bf16 caches)
+        // every V tile passes here in ring order (so this warp never runs a barrier phase ahead of the ring): a
+        // unit's last tile may hold cache rows past the tree block (junk, NaN possibly), which become zeros before
+        // any PV reads the tile, so that P = 0 there contributes exactly nothing (the 8-bit and 4-bit converters
+        // write those rows as zeros themselves)
+        if (!CONV && active) {
+            uint32_t n = 0;
+            bool ok = true;
+            SegIter si;
+            si.init(a, plan, UQ, QG, TG);
+            Seg sg;
+            while (ok && !*err && si.next(sg)) {
+                const int L = __ldg(a.kv_len + sg.b);
+                for (int t = sg.t0; t < sg.t1 && ok; ++t, ++n) {
+                    const uint32_t slot = n & 1;
+                    ok = __all_sync(0xffffffffu, mbar_wait(&sh.raw[2 + slot], (n >> 1) & 1, err));
+                    if (!ok) break;
+                    const int r_lo = L + T - t * kTileN;
+                    if (r_lo < kTileN) {
+                        uint8_t* vdst = smem + kSmemV + slot * kSlotBytes;
+                        for (int idx = lane; idx < (kTileN - r_lo) * 16; idx += 32) {
+                            const int rr = r_lo + (idx >> 4), c = idx & 15;
+                            *(uint4*)(vdst + (c >> 3) * kBoxBytes + sw128_offset(rr, c & 7)) = make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_smem();
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sh.full[2 + slot]);
+                }
+            }
+        }
     } else if (warp >= 12) {
         // ---------------------------------------------------------------- converters (8-bit / 4-bit caches)
         // converter ci (one per SM sub-partition) rewrites rows 32 ci .. 32 ci + 31 of every K and V tile, and a
@@ -653,12 +701,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         }
     } else if (warp >= 4 && active) {
         // ---------------------------------------------------------------- softmax warps
-        // Warp 4 + 4 side + q owns TMEM lane quadrant q (query rows 32q .. 32q+31 of the side's M tile).
+        // Warp 4 + 4 side + q owns TMEM lane quadrant q (query rows 32q .. 32q+31 of the side's M tile).  The
+        // segment walk and the pending epilogue live in shared memory (sh.sm[warp - 4]), so the tile loop keeps
+        // its registers for the scores.
         const int side = (warp - 4) >> 2;
         const int quad = warp & 3;
         const int row = quad * 32 + lane;        // query row inside the M tile (= TMEM lane)
         const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
         const uint32_t tS = tmem + lane_addr + col_S(side), tO = tmem + lane_addr + col_O(side);
+        SoftmaxState& ss = sh.sm[warp - 4];
+        if (lane == 0) {
+            ss.it.init(a, plan, UQ, QG, TG);
+            ss.pend_on = 0;
+        }
+        __syncwarp();
         uint32_t g = 0, nseg = 0, base = 0;
         // A warp that hits a time-out stops waiting and touching TMEM but keeps walking the segments, the
         // tiles and every barrier, so no partner is ever left waiting on it.
@@ -668,51 +724,49 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             return !dead;
         };
         auto all_sync = [&]() { asm volatile("bar.sync 1, 256;" ::: "memory"); };
-        // Epilogue of a finished segment, run after the side's first tile of the next segment (or at the end of
-        // the next segment when the side has no tile there): the softmax works on that tile while the segment's
-        // last PV completes.  O is normalised (bf16) into the output rows or the partial slot, then released.
-        struct Pending {
-            float m, l, sc, osc;
-            int b, hk, qg, rows;
-            uint8_t* part;
-            uint32_t nseg;
-            bool pair, on;
-        } pend;
-        pend.on = false;
+        // Epilogue of a finished segment, run after the side's first tile of the next segment (or at once when the
+        // side has no tile there): the softmax works on that tile while the segment's last PV completes.  O is
+        // normalised (bf16) into the output rows or the partial slot, then released.
         auto epilogue = [&]() {
-            const bool pr = pend.pair;
+            const Seg& pg = ss.pend;
+            const bool pr = pg.pair;
             const int urow = pr ? side * kRows + row : row;      // row inside the unit
-            const int qi = pend.qg * kUnitRows + urow;
-            const bool valid = urow < pend.rows;
+            const int qi = pg.qg * kUnitRows + urow;
+            const bool valid = urow < pg.rows;
             const int t_node = valid ? qi / G : 0, g_head = valid ? qi - t_node * G : 0;
-            const size_t out_row = ((size_t)pend.b * T + t_node) * a.Hq + (size_t)pend.hk * G + g_head;
-            const float m_log2 = pend.m == -INFINITY ? -INFINITY : pend.m * pend.sc;
-            float M = m_log2, Lsum = pend.l, wa = 1.f, wb = 0.f;
+            const size_t out_row = ((size_t)pg.b * T + t_node) * a.Hq + (size_t)pg.hk * G + g_head;
+            const float sc = CONV ? scale_log2 * __ldg(a.k_scale + pg.hk) : scale_log2;
+            const float osc = CONV ? __ldg(a.v_scale + pg.hk) : 1.f;
+            const float pm = sh.pm[side][row], pl = sh.pl[side][row];
+            const float m_log2 = pm == -INFINITY ? -INFINITY : pm * sc;
+            float M = m_log2, Lsum = pl, wa = 1.f, wb = 0.f;
             if (!pr) {
                 // split mode: both sides hold the same rows (A the even tiles, B the odd ones)
                 sh.ml[side][0][row] = m_log2;
-                sh.ml[side][1][row] = pend.l;
                 all_sync();
-                const float m0 = sh.ml[0][0][row], l0 = sh.ml[0][1][row], m1 = sh.ml[1][0][row], l1 = sh.ml[1][1][row];
+                const float m0 = sh.ml[0][0][row], l0 = sh.pl[0][row], m1 = sh.ml[1][0][row], l1 = sh.pl[1][row];
                 M = fmaxf(m0, m1);
                 wa = (M == -INFINITY || l0 == 0.f) ? 0.f : ex2(m0 - M);
                 wb = (M == -INFINITY || l1 == 0.f) ? 0.f : ex2(m1 - M);
                 Lsum = l0 * wa + l1 * wb;
-                all_sync();   // sh.ml may be rewritten by the next epilogue only after both sides read it
+                all_sync();   // sh.ml / sh.pl may be rewritten only after both sides read them
             }
-            if (wait(&sh.o_full[0], pend.nseg & 1) && wait(&sh.o_full[1], pend.nseg & 1)) tc_fence_after();
+            if (wait(&sh.o_full[0], ss.pend_nseg & 1) && wait(&sh.o_full[1], ss.pend_nseg & 1)) tc_fence_after();
             if (!dead) {
-                const float inv = Lsum > 0.f ? pend.osc / Lsum : 0.f;
+                const float inv = Lsum > 0.f ? osc / Lsum : 0.f;
+                uint8_t* part = pg.split ? (uint8_t*)a.ws + slots_off() + (long long)pg.slot * slot_bytes() : nullptr;
                 // pair mode: this side's whole row (d 0..127); split mode: side A d 0..63, side B d 64..127
                 const int d0 = pr ? 0 : 64 * side, nch = pr ? 8 : 4;
-                uint16_t* dst_row = pend.part ? (uint16_t*)pend.part + (size_t)urow * kD
-                                              : (uint16_t*)a.out + out_row * kD;
+                uint16_t* dst_row = part ? (uint16_t*)part + (size_t)urow * kD : (uint16_t*)a.out + out_row * kD;
+#pragma unroll 1
                 for (int c = 0; c < nch; ++c) {   // 16 columns at a time
                     uint32_t oa[16], ob[16];
                     __syncwarp();
                     tmem_ld16(tmem + lane_addr + col_O(pr ? side : 0) + d0 + 16 * c, oa);
                     if (!pr) tmem_ld16(tmem + lane_addr + col_O(1) + d0 + 16 * c, ob);
                     tmem_ld_wait();
+                    reg_fence(oa);
+                    if (!pr) reg_fence(ob);
                     if (valid) {
                         uint4* dst = (uint4*)(dst_row + d0 + 16 * c);
 #pragma unroll
@@ -734,8 +788,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                     }
                 }
                 if (valid && (pr || side == 0)) {
-                    if (pend.part) {
-                        float* ml = (float*)(pend.part + (size_t)kUnitRows * kD * 2);
+                    if (part) {
+                        float* ml = (float*)(part + (size_t)kUnitRows * kD * 2);
                         ml[urow] = M;
                         ml[kUnitRows + urow] = Lsum;
                     } else if (a.lse) {
@@ -745,32 +799,34 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 tc_fence_before();
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.o_free);
-            pend.on = false;
+            if (lane == 0) {
+                mbar_arrive(&sh.o_free);
+                ss.pend_on = 0;
+            }
+            __syncwarp();
         };
 
-        SegIter si;
-        si.init(a, plan, UQ, QG, TG);
-        Seg sg;
         bool first_seg = true;
-        while (si.next(sg)) {
-            const int b = sg.b, hk = sg.hk;
-            const int nt = sg.t1 - sg.t0;
+        for (;;) {
+            if (lane == 0) ss.has = ss.it.next(ss.seg) ? 1 : 0;
+            __syncwarp();
+            if (!ss.has) break;
+            const int b = ss.seg.b, hk = ss.seg.hk;
+            const int nt = ss.seg.t1 - ss.seg.t0, t0 = ss.seg.t0;
+            const bool pair = ss.seg.pair;
             const int L = __ldg(a.kv_len + b);
-            // softmax scale in log2 units (times k_scale for 8-bit / 4-bit K); output scale (v_scale)
+            // softmax scale in log2 units (times k_scale for 8-bit / 4-bit K)
             const float sc = CONV ? scale_log2 * __ldg(a.k_scale + hk) : scale_log2;
-            const float osc = CONV ? __ldg(a.v_scale + hk) : 1.f;
-            const int urow = sg.pair ? side * kRows + row : row;
-            const int qi = sg.qg * kUnitRows + urow;
-            const bool valid_row = urow < sg.rows;
+            const int urow = pair ? side * kRows + row : row;
+            const int qi = ss.seg.qg * kUnitRows + urow;
+            const bool valid_row = urow < ss.seg.rows;
             const int t_node = valid_row ? qi / G : 0;
-            uint8_t* part = sg.split ? (uint8_t*)a.ws + slots_off() + (long long)sg.slot * slot_bytes() : nullptr;
             dead = __any_sync(0xffffffffu, dead || *err);
             // Q written by the softmax warps when it is not loaded by TMA (G does not divide 128): this thread's row
             // (f16 for 8-bit / 4-bit caches), into the side's Q tile (pair mode) or tile A (split mode, side A)
             if (!q_tma) {
                 if (nseg > 0) wait(&sh.q_empty, (nseg - 1) & 1);
-                if (!dead && (sg.pair || side == 0)) {
+                if (!dead && (pair || side == 0)) {
                     const int gh = valid_row ? qi - t_node * G : 0;
                     const size_t qrow = ((size_t)b * T + t_node) * a.Hq + (size_t)hk * G + gh;
                     const uint4* src = (const uint4*)((const uint16_t*)a.q + qrow * kD);
@@ -783,7 +839,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                             v.z = bf16x2_to_f16x2(v.z);
                             v.w = bf16x2_to_f16x2(v.w);
                         }
-                        *(uint4*)(smem + kSmemQ + (sg.pair ? side : 0) * kSlotBytes + (d8 >> 3) * kBoxBytes +
+                        *(uint4*)(smem + kSmemQ + (pair ? side : 0) * kSlotBytes + (d8 >> 3) * kBoxBytes +
                                   sw128_offset(row, d8 & 7)) = v;
                     }
                     fence_proxy_async_smem();   // the MMAs (async proxy) read what this thread wrote
@@ -807,6 +863,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                          : "=r"(bad) : "r"(bad) : "memory");
             if (side == 0 && row == 0 && first_seg) {
                 // the unit that began in an earlier CTA's range and ends in this one is merged by attn_merge_kernel
+                const Seg& sg = ss.seg;
                 SplitRec rc;
                 rc.unit = (sg.s0 < plan.lo && sg.s1 <= plan.hi && !bad) ? sg.unit : -1;
                 rc.b = b;
@@ -831,62 +888,47 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 }
             }
 
-            const int my_tiles = side_tiles(sg.pair, nt, side);
+            const int my_tiles = side_tiles(pair, nt, side);
             float m_run = -INFINITY, l_run = 0.f;    // running max (raw score units) and sum of the row
-            for (int i = 0; i < my_tiles; ++i, ++g) {
-                const int j = side_tile(sg.pair, i, side);      // tile index inside the segment
-                const int tile0 = (sg.t0 + j) * kTileN;
+            // the previous segment's epilogue runs after this segment's first tile (outside the tile loop)
+            int i = 0;
+            for (;;) {
+            while (i < my_tiles) {
+                const int tile0 = (t0 + side_tile(pair, i, side)) * kTileN;
                 // the side's S tile is complete (and every earlier MMA of this CTA with it)
                 wait(&sh.s_full[side], g & 1);
                 tc_fence_after();
                 __syncwarp();
-                // bit c of allow[h]: column 64h + c is a prefix position or an ancestor of the row's node (anc has no
-                // bit >= T); padding rows allow nothing; only tiles that reach the tree block are masked
+                // bit e of the mask word of the 32 columns 32c..32c+31: a prefix position or an ancestor of the row's
+                // node (anc has no bit >= T); padding rows allow nothing; only tiles that reach the tree block are masked
                 const bool masked = tile0 + kTileN > L;
-                uint32_t allow[4] = {~0u, ~0u, ~0u, ~0u};
-                if (masked) {
+                auto allow_word = [&](int c) -> uint32_t {
+                    const int pos0 = tile0 + 32 * c;
+                    const int np = L - pos0, a0 = pos0 - L;
+                    const uint32_t pre = np >= 32 ? ~0u : np <= 0 ? 0u : (1u << np) - 1u;
+                    const uint32_t tree = a0 >= 64 ? 0u : a0 >= 0 ? (uint32_t)(anc >> a0) : a0 > -32 ? (uint32_t)(anc << -a0) : 0u;
+                    return valid_row ? (pre | tree) : 0u;
+                };
+                // pass 1: the row's max over the tile, 32 columns per TMEM load
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(tS + 32 * c, r);
+                    tmem_ld_wait();
+                    reg_fence(r);
+                    const uint32_t al = masked ? allow_word(c) : ~0u;
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int pos0 = tile0 + 64 * hh;
-                        const int np = L - pos0, a0 = pos0 - L;
-                        const uint64_t pre = np >= 64 ? ~0ull : np <= 0 ? 0ull : (1ull << np) - 1ull;
-                        const uint64_t tree = a0 >= 64 ? 0ull : a0 >= 0 ? (anc >> a0) : a0 > -64 ? (anc << -a0) : 0ull;
-                        const uint64_t al = valid_row ? (pre | tree) : 0ull;
-                        allow[2 * hh] = (uint32_t)al;
-                        allow[2 * hh + 1] = (uint32_t)(al >> 32);
+                    for (int q = 0; q < 4; ++q) {
+                        float v[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int k = q + 4 * e;
+                            v[e] = ((al >> k) & 1u) ? __uint_as_float(r[k]) : -INFINITY;
+                        }
+                        mx[q] = max3(mx[q], max3(v[0], v[1], v[2]), max3(max3(v[3], v[4], v[5]), v[6], v[7]));
                     }
                 }
-                // pass 1: the row's max over the tile (32 columns per TMEM load, the next load in flight); tiles inside
-                // the prefix take the variant without the mask
-                uint32_t ra[32], rb[32];
-                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                auto pass1 = [&](auto mask_tag) {
-                    constexpr bool MASK = decltype(mask_tag)::value;
-                    auto tile_max = [&](const uint32_t (&r)[32], uint32_t al) {
-                        float v[32];
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            v[e] = (!MASK || ((al >> e) & 1u)) ? __uint_as_float(r[e]) : -INFINITY;
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            mx[c] = max3(mx[c], max3(v[c], v[c + 4], v[c + 8]),
-                                         max3(max3(v[c + 12], v[c + 16], v[c + 20]), v[c + 24], v[c + 28]));
-                    };
-                    tmem_ld32(tS, ra);
-                    tmem_ld_wait();
-                    tmem_ld32(tS + 32, rb);
-                    tile_max(ra, allow[0]);
-                    tmem_ld_wait();
-                    tmem_ld32(tS + 64, ra);
-                    tile_max(rb, allow[1]);
-                    tmem_ld_wait();
-                    tmem_ld32(tS + 96, rb);
-                    tile_max(ra, allow[2]);
-                    tmem_ld_wait();
-                    tile_max(rb, allow[3]);
-                };
-                if (masked) pass1(std::true_type{});
-                else pass1(std::false_type{});
                 const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
                 // lazy rescaling: the row keeps its running max unless the tile's max exceeds it by more than 2^8
                 const float m_new = fmaxf(m_run, tmax);
@@ -900,6 +942,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                         uint32_t o[32];
                         tmem_ld32(tO + 32 * c, o);
                         tmem_ld_wait();
+                        reg_fence(o);
 #pragma unroll
                         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
                         tmem_st32(tO + 32 * c, o);
@@ -913,82 +956,59 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 const float moff = m_use != -INFINITY ? -m_use * sc : 0.f;
                 const uint64_t sc2 = f2pack(sc, sc), mo2 = f2pack(moff, moff);
                 uint64_t ps2[4] = {0ull, 0ull, 0ull, 0ull};
-                auto pass2 = [&](auto mask_tag) {
-                    constexpr bool MASK = decltype(mask_tag)::value;
-                    auto tile_p = [&](const uint32_t (&r)[32], uint32_t al, int c) {
-                        uint32_t pk[16];
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(tS + 32 * c, r);
+                    tmem_ld_wait();
+                    reg_fence(r);
+                    const uint32_t al = masked ? allow_word(c) : ~0u;
+                    uint32_t pk[16];
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float s0 = (!MASK || ((al >> (2 * e)) & 1u)) ? __uint_as_float(r[2 * e]) : -INFINITY;
-                            const float s1 = (!MASK || ((al >> (2 * e + 1)) & 1u)) ? __uint_as_float(r[2 * e + 1]) : -INFINITY;
-                            float x0, x1;
-                            f2unpack(f2fma(f2pack(s0, s1), sc2, mo2), x0, x1);
-                            const float p0 = ex2(x0), p1 = ex2(x1);
-                            ps2[e & 3] = f2add(ps2[e & 3], f2pack(p0, p1));
-                            pk[e] = pack2<CONV>(p0, p1);
-                        }
-                        if (!dead) tmem_st16(tS + 16 * c, pk);
-                    };
-                    tmem_ld32(tS, ra);
-                    tmem_ld_wait();
-                    tmem_ld32(tS + 32, rb);
-                    tile_p(ra, allow[0], 0);
-                    tmem_ld_wait();
-                    tmem_ld32(tS + 64, ra);
-                    tile_p(rb, allow[1], 1);
-                    tmem_ld_wait();
-                    tmem_ld32(tS + 96, rb);
-                    tile_p(ra, allow[2], 2);
-                    tmem_ld_wait();
-                    tile_p(rb, allow[3], 3);
-                };
-                if (masked) pass2(std::true_type{});
-                else pass2(std::false_type{});
+                    for (int e = 0; e < 16; ++e) {
+                        const float s0 = ((al >> (2 * e)) & 1u) ? __uint_as_float(r[2 * e]) : -INFINITY;
+                        const float s1 = ((al >> (2 * e + 1)) & 1u) ? __uint_as_float(r[2 * e + 1]) : -INFINITY;
+                        float x0, x1;
+                        f2unpack(f2fma(f2pack(s0, s1), sc2, mo2), x0, x1);
+                        const float p0 = ex2(x0), p1 = ex2(x1);
+                        ps2[e & 3] = f2add(ps2[e & 3], f2pack(p0, p1));
+                        pk[e] = pack2<CONV>(p0, p1);
+                    }
+                    if (!dead) tmem_st16(tS + 16 * c, pk);
+                }
                 float ps[4], ps_hi[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) f2unpack(ps2[q], ps[q], ps_hi[q]);
                 const float psum = ((ps[0] + ps_hi[0]) + (ps[1] + ps_hi[1])) + ((ps[2] + ps_hi[2]) + (ps[3] + ps_hi[3]));
                 l_run = (m_run == -INFINITY) ? psum : l_run * alpha + psum;
                 m_run = m_use;
-                // bf16 caches: the unit's last tile may hold cache rows past the tree block; the side that reads the
-                // tile first zeroes those V rows (NaN-safe) before its P is released
-                if (!CONV && !dead && tile0 + kTileN > L + T && (side == 0 || !sg.pair)) {
-                    const uint32_t ridx = base + (uint32_t)j;
-                    if (wait(&sh.full[2 + (ridx & 1)], (ridx >> 1) & 1)) {
-                        const int r_lo = max(0, L + T - tile0);
-                        uint8_t* vdst = smem + kSmemV + (ridx & 1) * kSlotBytes;
-                        for (int idx = quad * 32 + lane; idx < (kTileN - r_lo) * 16; idx += 128) {
-                            const int rr = r_lo + (idx >> 4), c = idx & 15;
-                            *(uint4*)(vdst + (c >> 3) * kBoxBytes + sw128_offset(rr, c & 7)) = make_uint4(0, 0, 0, 0);
-                        }
-                        fence_proxy_async_smem();
-                    }
-                }
                 if (!dead) {
                     tmem_st_wait();
                     tc_fence_before();
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sh.p_full[side]);
-                if (pend.on) epilogue();   // the previous segment's
+                ++i;
+                ++g;
+                if (ss.pend_on) break;
             }
-            if (pend.on) epilogue();       // the side had no tile in this segment
+            if (!ss.pend_on) break;
+            epilogue();                    // the previous segment's (at once if the side has no tile here)
+            }
             // this segment's epilogue waits until the side's first tile of the next segment is done
-            pend.m = m_run;
-            pend.l = l_run;
-            pend.sc = sc;
-            pend.osc = osc;
-            pend.b = b;
-            pend.hk = hk;
-            pend.qg = sg.qg;
-            pend.rows = sg.rows;
-            pend.part = part;
-            pend.pair = sg.pair;
-            pend.nseg = nseg++;
-            pend.on = true;
+            sh.pm[side][row] = m_run;
+            sh.pl[side][row] = l_run;
+            __syncwarp();
+            if (lane == 0) {
+                ss.pend = ss.seg;
+                ss.pend_nseg = nseg;
+                ss.pend_on = 1;
+            }
+            __syncwarp();
+            ++nseg;
             base += (uint32_t)nt;
         }
-        if (pend.on) epilogue();
+        if (ss.pend_on) epilogue();
     }
     if (!active && tid == 0) {   // CTAs beyond the used grid complete no split unit
         SplitRec r = {};
@@ -1014,7 +1034,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 constexpr int kMergeRows = 16;
 constexpr int kMergeUnits = kUnitRows / kMergeRows;   // per record
 
-__global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(AttnArgs a, int grid_main) {
+__global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const __grid_constant__ AttnArgs a, int grid_main) {
     __shared__ int s_bad;
     const int T = a.T, G = a.Hq / a.Hkv;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1071,6 +1091,25 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(AttnArgs a, i
         const int cl = u / kMergeUnits, rb = u - cl * kMergeUnits;
         const SplitRec rec = recs[cl];
         if (rec.unit < 0 || rec.rows <= rb * kMergeRows) continue;
+        // a request that fails validation keeps the zero outputs of step 1 (checked here again: step 1 may run in
+        // another CTA, before or after this one)
+        if (tid == 0) s_bad = 0;
+        __syncthreads();
+        {
+            const int L = __ldg(a.kv_len + rec.b);
+            if (tid < T) {
+                const int p = __ldg(a.parent + (size_t)rec.b * T + tid);
+                if (tid == 0 ? p != -1 : (p < 0 || p >= tid)) s_bad = 1;
+            }
+            if (L < 0 || L + T > a.kv_cap) s_bad = 1;
+            else if (a.page_table) {
+                const int32_t* pt = a.page_table + (size_t)rec.b * a.max_pages;
+                for (int i = tid; i <= (L + T - 1) >> a.page_shift; i += blockDim.x)
+                    if (__ldg(pt + i) < 0 || __ldg(pt + i) >= a.num_pages) s_bad = 1;
+            }
+        }
+        __syncthreads();
+        if (s_bad) continue;
         float m[2][4], l[2][4];
         uint2 x[2][4];
         int rr[2];
