@@ -17,12 +17,11 @@
 namespace sv {
 namespace tc {
 
-// Waits on an mbarrier sleep in hardware until the phase completes (try_wait with a suspend-time hint, so a
-// waiting warp does not steal issue slots from the warps doing the work) and give up after kSpinLimit
-// tries of at most kSuspendNs each (about one second in all): a lost arrival ends the kernel with an error
-// instead of hanging the GPU.
-constexpr uint32_t kSpinLimit = 1u << 12;
-constexpr uint32_t kSuspendNs = 250000;
+// Waits on an mbarrier: try_wait without a suspend-time hint (the hardware suspends the thread for a short,
+// system-dependent time and wakes it when the phase completes), repeated until the phase completes or about
+// kWaitCycles SM clocks (about one second) have passed: a lost arrival ends the kernel with an error instead of
+// hanging the GPU.
+constexpr long long kWaitCycles = 1LL << 31;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -41,10 +40,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
+        : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return ok != 0;
 }
@@ -62,12 +61,12 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 }
 // Bounded wait for the phase with the given parity to complete; false (and *err set) on time-out.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* err) {
-    // a phase that has already completed is seen by the non-blocking test at once; try_wait with a
-    // suspend-time hint can hold the warp well past that
     if (mbar_test_wait(bar, parity)) return true;
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    const long long t0 = clock64();
+    for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*err) return false;   // another role already gave up
+        if (clock64() - t0 > kWaitCycles) break;
     }
     *err = 1;
     return false;
