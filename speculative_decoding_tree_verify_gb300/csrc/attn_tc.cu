@@ -909,26 +909,32 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                     const uint32_t tree = a0 >= 64 ? 0u : a0 >= 0 ? (uint32_t)(anc >> a0) : a0 > -32 ? (uint32_t)(anc << -a0) : 0u;
                     return valid_row ? (pre | tree) : 0u;
                 };
-                // pass 1: the row's max over the tile, 32 columns per TMEM load
+                // pass 1: the row's max over the tile, 32 columns per TMEM load (tiles inside the prefix take the
+                // variant without the mask)
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                auto pass1 = [&](auto mask_tag) {
+                    constexpr bool MASK = decltype(mask_tag)::value;
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(tS + 32 * c, r);
-                    tmem_ld_wait();
-                    reg_fence(r);
-                    const uint32_t al = masked ? allow_word(c) : ~0u;
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(tS + 32 * c, r);
+                        tmem_ld_wait();
+                        reg_fence(r);
+                        const uint32_t al = MASK ? allow_word(c) : ~0u;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        float v[8];
+                        for (int q = 0; q < 4; ++q) {
+                            float v[8];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int k = q + 4 * e;
-                            v[e] = ((al >> k) & 1u) ? __uint_as_float(r[k]) : -INFINITY;
+                            for (int e = 0; e < 8; ++e) {
+                                const int k = q + 4 * e;
+                                v[e] = (!MASK || ((al >> k) & 1u)) ? __uint_as_float(r[k]) : -INFINITY;
+                            }
+                            mx[q] = max3(mx[q], max3(v[0], v[1], v[2]), max3(max3(v[3], v[4], v[5]), v[6], v[7]));
                         }
-                        mx[q] = max3(mx[q], max3(v[0], v[1], v[2]), max3(max3(v[3], v[4], v[5]), v[6], v[7]));
                     }
-                }
+                };
+                if (masked) pass1(std::true_type{});
+                else pass1(std::false_type{});
                 const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
                 // lazy rescaling: the row keeps its running max unless the tile's max exceeds it by more than 2^8
                 const float m_new = fmaxf(m_run, tmax);
@@ -956,26 +962,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 const float moff = m_use != -INFINITY ? -m_use * sc : 0.f;
                 const uint64_t sc2 = f2pack(sc, sc), mo2 = f2pack(moff, moff);
                 uint64_t ps2[4] = {0ull, 0ull, 0ull, 0ull};
+                auto pass2 = [&](auto mask_tag) {
+                    constexpr bool MASK = decltype(mask_tag)::value;
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(tS + 32 * c, r);
-                    tmem_ld_wait();
-                    reg_fence(r);
-                    const uint32_t al = masked ? allow_word(c) : ~0u;
-                    uint32_t pk[16];
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(tS + 32 * c, r);
+                        tmem_ld_wait();
+                        reg_fence(r);
+                        const uint32_t al = MASK ? allow_word(c) : ~0u;
+                        uint32_t pk[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float s0 = ((al >> (2 * e)) & 1u) ? __uint_as_float(r[2 * e]) : -INFINITY;
-                        const float s1 = ((al >> (2 * e + 1)) & 1u) ? __uint_as_float(r[2 * e + 1]) : -INFINITY;
-                        float x0, x1;
-                        f2unpack(f2fma(f2pack(s0, s1), sc2, mo2), x0, x1);
-                        const float p0 = ex2(x0), p1 = ex2(x1);
-                        ps2[e & 3] = f2add(ps2[e & 3], f2pack(p0, p1));
-                        pk[e] = pack2<CONV>(p0, p1);
+                        for (int e = 0; e < 16; ++e) {
+                            const float s0 = (!MASK || ((al >> (2 * e)) & 1u)) ? __uint_as_float(r[2 * e]) : -INFINITY;
+                            const float s1 = (!MASK || ((al >> (2 * e + 1)) & 1u)) ? __uint_as_float(r[2 * e + 1]) : -INFINITY;
+                            float x0, x1;
+                            f2unpack(f2fma(f2pack(s0, s1), sc2, mo2), x0, x1);
+                            const float p0 = ex2(x0), p1 = ex2(x1);
+                            ps2[e & 3] = f2add(ps2[e & 3], f2pack(p0, p1));
+                            pk[e] = pack2<CONV>(p0, p1);
+                        }
+                        if (!dead) tmem_st16(tS + 16 * c, pk);
                     }
-                    if (!dead) tmem_st16(tS + 16 * c, pk);
-                }
+                };
+                if (masked) pass2(std::true_type{});
+                else pass2(std::false_type{});
                 float ps[4], ps_hi[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) f2unpack(ps2[q], ps[q], ps_hi[q]);
