@@ -67,6 +67,16 @@ const char* sv_status_string(sv_status s);
 int sv_version(void);
 
 /*
+ * sv_set_wait_limit -- diagnostic: how long a bounded wait of the tensor-core attention kernels tries before it
+ * gives up, in SM clock cycles (0 restores the default, 2^31: about one second).  No kernel of the library ever
+ * waits without a bound: a lost arrival ends the wait, the kernel winds down (waiting with the full limit for its
+ * own copies and MMAs) and every request of the call gets SV_ERR_TIMEOUT.  A tiny limit makes those waits give up
+ * at once, so a test can drive the failure path without faulting or hanging the GPU.  Process-wide setting read
+ * when a call is launched (a CUDA graph keeps the value it was captured with); negative values are rejected.
+ */
+sv_status sv_set_wait_limit(long long sm_cycles);
+
+/*
  * Bytes of device workspace a call needs (0 if none).  Arguments that do not apply to `op` are ignored:
  *   SV_OP_TREE_ATTN: B, T, Hq, Hkv, D, kv_cap      SV_OP_ACCEPT: B (= rows/T), T, V      SV_OP_LOSS: B (= N), T, V
  *   SV_OP_TREE_ATTN_BWD: B, T, Hq

@@ -69,8 +69,14 @@ constexpr int kMergeThreads = 256;               // 8 warps
 // Raw 8-bit tiles land in box 1 of their slot (bytes 16 KB..32 KB), raw 4-bit codes at 24 KB..32 KB with their
 // block scales at 23 KB..24 KB; the converters rewrite the slot as two f16 boxes.
 constexpr int kSmemQ = 0;
-constexpr int kSmemK = 2 * kSlotBytes;
 constexpr int kSmemV = 4 * kSlotBytes;
+// KS K slots: 2 (Q holds two M tiles), or 3 when every unit of the launch is in split mode (one M tile of Q, and
+// the second tile's 32 KB holds a third K slot, so K is prefetched two tiles ahead)
+template <int KS>
+__host__ __device__ constexpr int smem_k() { return KS == 3 ? kSlotBytes : 2 * kSlotBytes; }
+// ring positions: the n-th K tile in slot n % KS (barrier index = slot), the n-th V tile in slot n % 2 (barrier
+// index 3 + slot)
+constexpr int kVBar = 3;
 constexpr int kSmemBytes = 6 * kSlotBytes;       // 196608
 constexpr int kSmemAlloc = kSmemBytes + 1024;    // + alignment slack
 constexpr int kRaw8Off = kBoxBytes;              // e4m3 tile: [128 rows][128 B], 128-byte swizzle
@@ -346,7 +352,7 @@ struct SoftmaxState {
 };
 
 struct MainShared {
-    uint64_t full[4], raw[4], empty[4];                    // K slots 0, 1 and V slots 2, 3
+    uint64_t full[5], raw[5], empty[5];                    // K slots 0 .. KS-1 and V slots 3, 4
     uint64_t s_full[2], p_full[2], o_full[2];              // per side
     uint64_t o_free;                                       // the segment's O has been read by both sides
     uint64_t q_full, q_ready, q_empty, drain[2];
@@ -364,7 +370,7 @@ struct MainShared {
 // KVK: bf16, e4m3 or e2m1 caches.  8-bit and 4-bit caches are converted exactly to f16 and the MMAs run on f16
 // operands (Q rounded to f16); the per-kv-head scale of K is folded into the softmax scale and that of V into
 // the epilogue.
-template <int KVK>
+template <int KVK, int KS>
 __global__ void __launch_bounds__(threads_of<KVK>(), 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKs,
@@ -375,13 +381,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     __shared__ MainShared sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr int kSmemK = smem_k<KS>();
     const uint32_t sQ = smem_u32(smem + kSmemQ), sK = smem_u32(smem + kSmemK), sV = smem_u32(smem + kSmemV);
     const int T = a.T, G = a.Hq / a.Hkv, TG = T * G;
     const int QG = (TG + kUnitRows - 1) / kUnitRows, UQ = a.Hkv * QG;
     const int nbox = kTileN / box_rows;
 
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 5; ++i) {
             // K (bf16): the TMA transaction; V (bf16): the V cleaner; 8-bit / 4-bit: one arrival per converter warp
             mbar_init(&sh.full[i], CONV ? 4 : 1);
             mbar_init(&sh.raw[i], 1);                // the raw tile's TMA transaction
@@ -435,7 +442,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 if (kv == 0 && q_tma) {
                     // Q of the segment's M tile(s) (128 query rows = 128/G nodes x G heads each) once the previous
                     // segment's S MMAs no longer read it
-                    if (nseg > 0 && !mbar_wait(&sh.q_empty, (nseg - 1) & 1, err)) break;
+                    if (nseg > 0 && !mbar_wait(&sh.q_empty, (nseg - 1) & 1, err, a.wait_cycles)) break;
                     const int mt = sg.pair ? 2 : 1;
                     mbar_arrive_expect_tx(&sh.q_full, mt * 2 * kBoxBytes);
                     for (int m = 0; m < mt; ++m) {
@@ -447,9 +454,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 }
                 ++nseg;
                 for (int t = sg.t0; t < sg.t1 && !*err; ++t, ++n) {
-                    const uint32_t slot = n & 1, round = n >> 1;
-                    const uint32_t gslot = 2 * kv + slot;
-                    if (!mbar_wait(&sh.empty[gslot], (round & 1) ^ 1, err)) break;
+                    const uint32_t slot = kv ? n & 1 : n % KS, round = kv ? n >> 1 : n / KS;
+                    const uint32_t gslot = kv ? kVBar + slot : slot;
+                    if (!mbar_wait(&sh.empty[gslot], (round & 1) ^ 1, err, a.wait_cycles)) break;
                     uint8_t* dst = smem + (kv ? kSmemV : kSmemK) + slot * kSlotBytes;
                     if constexpr (KVK == KV_BF16) {
                         // K tiles go straight to the MMAs; V tiles pass the V cleaner first
@@ -474,11 +481,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                     }
                 }
             }
-            // wait (bounded) until the last slots have been released, so no copy is still in flight towards this
-            // CTA when it exits
+            // wait until the copies this thread issued have landed (their transaction barriers complete whatever the
+            // consumers do), so no copy is still in flight towards this CTA when it exits; these waits keep the full
+            // limit even when the work waits were given a short one
             volatile int local = 0;
-            for (uint32_t m = n > 2 ? n - 2 : 0; m < n && !local; ++m)
-                mbar_wait(&sh.empty[2 * kv + (m & 1)], (m >> 1) & 1, &local);
+            const uint32_t ns = kv ? 2u : (uint32_t)KS;
+            for (uint32_t m = n > ns ? n - ns : 0; m < n && !local; ++m) {
+                const uint32_t sl = kv ? m & 1 : m % KS, rd = kv ? m >> 1 : m / KS;
+                const bool tx_on_raw = CONV || kv;   // 8-bit / 4-bit tiles and bf16 V tiles land on raw, bf16 K on full
+                mbar_wait(tx_on_raw ? &sh.raw[kv ? kVBar + sl : sl] : &sh.full[sl], rd & 1, &local);
+            }
             if (kv == 0 && q_tma && nseg > 0 && !local) mbar_wait(&sh.q_full, (nseg - 1) & 1, &local);
         }
     } else if (warp == 1) {
@@ -498,8 +510,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             // S_X = Q_X K(tile)^T; commit to s_full_X (and release the K slot when `release`)
             // (split mode: both sides multiply Q tile A)
             auto issue_s = [&](int side, uint32_t ridx, bool release, bool pair) -> bool {
-                const uint32_t slot = ridx & 1;
-                if (!mbar_wait(&sh.full[slot], (ridx >> 1) & 1, err)) return false;
+                const uint32_t slot = ridx % KS;
+                if (!mbar_wait(&sh.full[slot], (ridx / KS) & 1, err, a.wait_cycles)) return false;
                 tc_fence_after();
                 const uint32_t kb = sK + slot * kSlotBytes, qb = sQ + (pair ? (uint32_t)side : 0u) * kSlotBytes;
 #pragma unroll
@@ -513,22 +525,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             // O_X += P_X V(tile) (P in the side's S columns); release the V slot when `release`
             auto issue_pv = [&](int side, uint32_t ridx, bool first, bool release) -> bool {
                 const uint32_t slot = ridx & 1;
-                if (!mbar_wait(&sh.full[2 + slot], (ridx >> 1) & 1, err)) return false;
-                if (!mbar_wait(&sh.p_full[side], g[side] & 1, err)) return false;
+                if (!mbar_wait(&sh.full[kVBar + slot], (ridx >> 1) & 1, err, a.wait_cycles)) return false;
+                if (!mbar_wait(&sh.p_full[side], g[side] & 1, err, a.wait_cycles)) return false;
                 tc_fence_after();
                 const uint32_t vb = sV + slot * kSlotBytes;
 #pragma unroll
                 for (int kk = 0; kk < kTileN / 16; ++kk)
                     mma_f16_ts(tmem + col_O(side), tmem + col_S(side) + kk * 8, at(dV, vb + kk * 2048), idO,
                                (!first || kk > 0) ? 1u : 0u);
-                if (release) mma_commit(&sh.empty[2 + slot]);
+                if (release) mma_commit(&sh.empty[kVBar + slot]);
                 ++g[side];
                 return true;
             };
             while (ok && !*err && si.next(sg)) {
                 const int nt = sg.t1 - sg.t0;
                 const int n0 = side_tiles(sg.pair, nt, 0), n1 = side_tiles(sg.pair, nt, 1);
-                ok = mbar_wait(qbar_ready ? &sh.q_ready : &sh.q_full, nseg & 1, err);
+                ok = mbar_wait(qbar_ready ? &sh.q_ready : &sh.q_full, nseg & 1, err, a.wait_cycles);
                 if (!ok) break;
                 tc_fence_after();
                 const bool rel0 = !sg.pair;                // pair mode: side B is a tile's last reader
@@ -541,7 +553,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                         const int ns = side ? n1 : n0;
                         if (i >= ns) continue;
                         if (!o_waited) {   // the previous segment's epilogue has read O_A and O_B
-                            ok = mbar_wait(&sh.o_free, (nseg - 1) & 1, err);
+                            ok = mbar_wait(&sh.o_free, (nseg - 1) & 1, err, a.wait_cycles);
                             if (!ok) break;
                             tc_fence_after();
                             o_waited = true;
@@ -580,7 +592,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 const int L = __ldg(a.kv_len + sg.b);
                 for (int t = sg.t0; t < sg.t1 && ok; ++t, ++n) {
                     const uint32_t slot = n & 1;
-                    ok = __all_sync(0xffffffffu, mbar_wait(&sh.raw[2 + slot], (n >> 1) & 1, err));
+                    ok = __all_sync(0xffffffffu, mbar_wait(&sh.raw[kVBar + slot], (n >> 1) & 1, err, a.wait_cycles));
                     if (!ok) break;
                     const int r_lo = L + T - t * kTileN;
                     if (r_lo < kTileN) {
@@ -592,7 +604,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                         fence_proxy_async_smem();
                     }
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&sh.full[2 + slot]);
+                    if (lane == 0) mbar_arrive(&sh.full[kVBar + slot]);
                 }
             }
         }
@@ -610,7 +622,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             while (ok && !*err && si.next(sg)) {
                 const int L = __ldg(a.kv_len + sg.b);
                 if (q_tma) {
-                    ok = __all_sync(0xffffffffu, mbar_wait(&sh.q_full, nseg & 1, err));
+                    ok = __all_sync(0xffffffffu, mbar_wait(&sh.q_full, nseg & 1, err, a.wait_cycles));
                     if (!ok) break;
                     const int nq = (sg.pair ? 2 : 1) * kSlotBytes / 16;   // 16-byte chunks of Q
                     for (int c = ci * 32 + lane; c < nq; c += 128) {
@@ -628,10 +640,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 ++nseg;
                 for (int t = sg.t0; t < sg.t1 && ok; ++t, ++n) {
                     for (int kv = 0; kv < 2 && ok; ++kv) {
-                        const uint32_t gslot = 2 * kv + (n & 1), round = n >> 1;
-                        ok = __all_sync(0xffffffffu, mbar_wait(&sh.raw[gslot], round & 1, err));
+                        const uint32_t sl = kv ? n & 1 : n % KS, round = kv ? n >> 1 : n / KS;
+                        const uint32_t gslot = kv ? kVBar + sl : sl;
+                        ok = __all_sync(0xffffffffu, mbar_wait(&sh.raw[gslot], round & 1, err, a.wait_cycles));
                         if (!ok) break;
-                        uint8_t* slot = smem + (kv ? kSmemV : kSmemK) + (n & 1) * kSlotBytes;
+                        uint8_t* slot = smem + (kv ? kSmemV : kSmemK) + sl * kSlotBytes;
                         // V rows past the tree block hold junk (NaN possibly): they become zeros, so that P = 0 there
                         // contributes exactly nothing
                         const bool zero = kv == 1 && t * kTileN + r >= L + T;
@@ -667,7 +680,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                             // so a converter that gave up cannot leave the others waiting forever)
                             __syncwarp();
                             if (lane == 0) mbar_arrive(&sh.conv_bar);
-                            ok = __all_sync(0xffffffffu, mbar_wait(&sh.conv_bar, nconv & 1, err));
+                            ok = __all_sync(0xffffffffu, mbar_wait(&sh.conv_bar, nconv & 1, err, a.wait_cycles));
                             ++nconv;
                             if (!ok) break;
                             uint32_t s16[8];   // block scales as f16, each broadcast to a pair
@@ -720,7 +733,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         // tiles and every barrier, so no partner is ever left waiting on it.
         bool dead = false;
         auto wait = [&](uint64_t* bar, uint32_t parity) {
-            if (!dead) dead = __any_sync(0xffffffffu, !mbar_wait(bar, parity, err));
+            if (!dead) dead = __any_sync(0xffffffffu, !mbar_wait(bar, parity, err, a.wait_cycles));
             return !dead;
         };
         auto all_sync = [&]() { asm volatile("bar.sync 1, 256;" ::: "memory"); };
@@ -1239,12 +1252,12 @@ long long view_rows(const AttnArgs& a) {
 
 // CTAs that fit on the device at once with this kernel's resources (cached per kernel); the persistent grid
 // never exceeds it, so every CTA of the grid is resident from the start.
-template <int KVK>
+template <int KVK, int KS>
 int resident_ctas() {
     static int n = 0;
     if (!n) {
         int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_tc_kernel<KVK>, threads_of<KVK>(), kSmemAlloc) !=
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_tc_kernel<KVK, KS>, threads_of<KVK>(), kSmemAlloc) !=
                 cudaSuccess || per_sm < 1)
             per_sm = 1;
         n = per_sm * num_sms();
@@ -1252,11 +1265,11 @@ int resident_ctas() {
     return n;
 }
 
-template <int KVK>
+template <int KVK, int KS>
 cudaError_t launch_main(const AttnArgs& a, cudaStream_t s, float scale_log2, int* grid_out) {
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<KVK>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<KVK, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -1285,11 +1298,20 @@ cudaError_t launch_main(const AttnArgs& a, cudaStream_t s, float scale_log2, int
     // Q by TMA when the heads of a kv group tile the 128-row M tile; else the softmax warps write it
     const int q_tma = encode_q_map(&tmQ, a) ? 1 : 0;
     if (!q_tma) tmQ = tmK;
-    int grid = resident_ctas<KVK>();
+    int grid = resident_ctas<KVK, KS>();
     if (grid > kMaxGrid) grid = kMaxGrid;
     *grid_out = grid;
-    return launch_ex(attn_tc_kernel<KVK>, dim3(grid), dim3(threads_of<KVK>()), (size_t)kSmemAlloc, s, 1, false, tmK,
-                     tmV, tmQ, tmKs, tmVs, a, scale_log2, q_tma, (int)box_rows);
+    AttnArgs la = a;
+    la.wait_cycles = attn_wait_cycles();
+    return launch_ex(attn_tc_kernel<KVK, KS>, dim3(grid), dim3(threads_of<KVK>()), (size_t)kSmemAlloc, s, 1, false, tmK,
+                     tmV, tmQ, tmKs, tmVs, la, scale_log2, q_tma, (int)box_rows);
+}
+
+// every unit of the launch in split mode (at most 128 query rows per kv head): the 3-slot K ring
+template <int KVK>
+cudaError_t launch_kind(const AttnArgs& a, cudaStream_t s, float scale_log2, int* grid_out) {
+    const bool split_only = (long long)a.T * (a.Hq / a.Hkv) <= kRows;
+    return split_only ? launch_main<KVK, 3>(a, s, scale_log2, grid_out) : launch_main<KVK, 2>(a, s, scale_log2, grid_out);
 }
 
 }  // namespace
@@ -1319,9 +1341,9 @@ cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t s) {
     const float sl2 = scale * 1.4426950408889634f;
     int grid = 0;
     switch (kv_kind(a)) {
-    case KV_E4M3: e = launch_main<KV_E4M3>(a, s, sl2, &grid); break;
-    case KV_E2M1: e = launch_main<KV_E2M1>(a, s, sl2, &grid); break;
-    default: e = launch_main<KV_BF16>(a, s, sl2, &grid); break;
+    case KV_E4M3: e = launch_kind<KV_E4M3>(a, s, sl2, &grid); break;
+    case KV_E2M1: e = launch_kind<KV_E2M1>(a, s, sl2, &grid); break;
+    default: e = launch_kind<KV_BF16>(a, s, sl2, &grid); break;
     }
     if (e != cudaSuccess) return e;
     return launch_ex(attn_merge_kernel, dim3(grid * kMergeUnits), dim3(kMergeThreads), 0, s, 1, true, a, grid);

@@ -2,6 +2,8 @@
 // Semantics, layouts and error behaviour are documented in include/sv.h.
 #include <math.h>
 
+#include <atomic>
+
 #include "sv_internal.cuh"
 
 using namespace sv;
@@ -9,6 +11,15 @@ using namespace sv;
 namespace {
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+constexpr long long kDefaultWaitCycles = 1LL << 31;   // about one second at the GB300's clocks
+std::atomic<long long> g_wait_cycles{kDefaultWaitCycles};
+
+}  // namespace
+
+long long sv::attn_wait_cycles() { return g_wait_cycles.load(); }
+
+namespace {
 
 // Most of the work is asynchronous; a failed launch surfaces here.
 sv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SV_OK : SV_ERR_CUDA; }
@@ -33,6 +44,12 @@ const char* sv_status_string(sv_status s) {
 }
 
 int sv_version(void) { return 100; }
+
+sv_status sv_set_wait_limit(long long sm_cycles) {
+    if (sm_cycles < 0) return SV_ERR_INVALID_ARG;
+    g_wait_cycles.store(sm_cycles == 0 ? kDefaultWaitCycles : sm_cycles);
+    return SV_OK;
+}
 
 size_t sv_workspace_size(sv_op op, int B, int T, int Hq, int Hkv, int D, int kv_cap, int V) {
     if (B < 0 || T < 1 || T > SV_MAX_T) return 0;

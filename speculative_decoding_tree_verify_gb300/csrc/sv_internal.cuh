@@ -84,7 +84,11 @@ struct AttnArgs {
     int page_shift = 0;   // log2(page_size)
     int max_pages = 0;
     int num_pages = 0;
+    // SM clock cycles a bounded wait of the attention kernel tries before it gives up (sv_set_wait_limit)
+    long long wait_cycles = 1LL << 31;
 };
+
+long long attn_wait_cycles();
 
 size_t attn_workspace_size(int B, int T, int Hq, int Hkv, int D, int kv_cap);
 bool attn_tc_supported(const AttnArgs& a);

@@ -59,14 +59,16 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait for the phase with the given parity to complete; false (and *err set) on time-out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* err) {
+// Bounded wait for the phase with the given parity to complete; false (and *err set) on time-out after `limit`
+// SM clock cycles.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* err,
+                                          long long limit = kWaitCycles) {
     if (mbar_test_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*err) return false;   // another role already gave up
-        if (clock64() - t0 > kWaitCycles) break;
+        if (clock64() - t0 > limit) break;
     }
     *err = 1;
     return false;

@@ -39,6 +39,8 @@ def lib() -> C.CDLL:
         L.sv_status_string.argtypes = [i]
         L.sv_status_string.restype = C.c_char_p
         L.sv_version.restype = i
+        L.sv_set_wait_limit.argtypes = [C.c_longlong]
+        L.sv_set_wait_limit.restype = i
         L.sv_workspace_size.argtypes = [i] * 8
         L.sv_workspace_size.restype = z
         L.sv_tree_attn.argtypes = [i, i, i, i, i, i, i, i, P, P, P, P, P, P, P, f, P, P, P, P, z, P]
@@ -61,6 +63,11 @@ def lib() -> C.CDLL:
         L.sv_tree_expand.restype = i
         _lib = L
     return _lib
+
+
+def set_wait_limit(sm_cycles: int) -> None:
+    """sv_set_wait_limit: bounded-wait limit of the attention kernels in SM cycles (0 = default, about 1 s)."""
+    _check(lib().sv_set_wait_limit(int(sm_cycles)), "sv_set_wait_limit")
 
 
 def status_string(code: int) -> str:
