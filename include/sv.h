@@ -103,10 +103,11 @@ size_t sv_workspace_size(sv_op op, int B, int T, int Hq, int Hkv, int D, int kv_
  *   out      [B, T, Hq, D] in q_dt
  *   lse      float [B, T, Hq] or NULL
  *   status   int32 [B] or NULL; a failed request's out/lse rows are zero
- *   workspace / ws_bytes: at least sv_workspace_size(SV_OP_TREE_ATTN, ...) bytes, 256-byte aligned
+ *   workspace / ws_bytes: at least sv_workspace_size(SV_OP_TREE_ATTN, ...) bytes, 256-byte aligned; any
+ *            content (every call writes what it reads back); never shared by two calls that may overlap
  * Cache positions >= kv_len[b] + T are never used, whatever they hold (NaN included).
- * Shapes: 1 <= T <= 64, Hq % Hkv == 0, D in {64, 128} for the tensor-core path (other D up to 256 run
- * on the CUDA-core path), Hq / Hkv * T <= 512.
+ * Shapes: 1 <= T <= 64, Hq % Hkv == 0.  The tensor-core path takes bf16 Q with bf16 or E4M3 caches and
+ * D = 128; everything else (f32 tensors, D up to 256 with Hq / Hkv * D <= 4096) runs on the CUDA-core path.
  */
 sv_status sv_tree_attn(int B, int T, int Hq, int Hkv, int D, int kv_cap, sv_dtype q_dt, sv_dtype kv_dt,
                        const void* q, const void* k_cache, const void* v_cache, const float* k_scale,

@@ -1051,55 +1051,79 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 }
 
 // ------------------------------------------------------------------------------------------------ merge kernel
-// Runs after attn_tc_kernel (programmatic dependent launch): validates every request (statuses, zero outputs for
-// failed ones) and merges the segments of every unit that crossed a CTA range boundary.  One merge unit =
-// (record of CTA c, 16 rows): each warp merges two rows, lanes covering 4 of the 128 dims (coalesced 8-byte
-// loads), with every load of a row issued before any of them is used.
-constexpr int kMergeRows = 16;
-constexpr int kMergeUnits = kUnitRows / kMergeRows;   // per record
+// Runs after attn_tc_kernel (programmatic dependent launch), on a grid that is resident at once.  Before the
+// attention grid has completed, CTA x checks requests x, x + grid, ... (parent array, kv_len, page table: inputs
+// only).  Afterwards every CTA reads all the records (one load round), lists the 32-row chunks of the split units
+// in record order, and merges chunks x, x + grid, ...; CTAs x < B also write the statuses of their requests and
+// zero the outputs of failed ones.  A merge thread takes 16 dims of one row (8 threads per row, two 16-byte loads
+// per partial) and loads a batch of four contributors at once, so a unit spanning up to four CTAs costs one more
+// round of loads.
+constexpr int kMergeRows = kMergeThreads / 8;          // 32
+constexpr int kMergeBatch = 4;
+
+__device__ __forceinline__ int request_status(const AttnArgs& a, int b, int* s_flag) {
+    const int T = a.T, tid = threadIdx.x;
+    if (tid == 0) *s_flag = 0;
+    __syncthreads();
+    const int L = __ldg(a.kv_len + b);
+    if (tid < T) {
+        const int p = __ldg(a.parent + (size_t)b * T + tid);
+        if (tid == 0 ? p != -1 : (p < 0 || p >= tid)) *s_flag = 1;
+    }
+    __syncthreads();
+    int st = *s_flag ? SV_ERR_BAD_TREE : SV_OK;
+    if (st == SV_OK && (L < 0 || L + T > a.kv_cap)) st = SV_ERR_INVALID_ARG;
+    if (st == SV_OK && a.page_table) {   // every page the request reads must name a page of the pool
+        const int32_t* pt = a.page_table + (size_t)b * a.max_pages;
+        for (int i = tid; i <= (L + T - 1) >> a.page_shift; i += blockDim.x)
+            if (__ldg(pt + i) < 0 || __ldg(pt + i) >= a.num_pages) *s_flag = 2;
+        __syncthreads();
+        if (*s_flag) st = SV_ERR_INVALID_ARG;
+    }
+    __syncthreads();
+    return st;
+}
 
 __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const __grid_constant__ AttnArgs a, int grid_main) {
-    __shared__ int s_bad;
+    __shared__ int s_flag, s_to;
+    __shared__ SplitRec s_rec[kMaxGrid];
+    __shared__ int s_pfx[kMaxGrid + 1];   // chunks of the records before record c
+    __shared__ long long s_scan[33];
     const int T = a.T, G = a.Hq / a.Hkv;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    pdl_wait_prior();   // attention results are visible from here on
-    const SplitRec* recs = (const SplitRec*)((const uint8_t*)a.ws + rec_off());
-    // the time-out flags matter only to the CTAs that write statuses: after a time-out every status says so and
-    // the merged outputs (garbage then) are never read
-    bool timeout = false;
-    if ((int)blockIdx.x < a.B) {
-        if (tid == 0) s_bad = 0;
-        __syncthreads();
-        for (int c = tid; c < grid_main; c += blockDim.x)
-            if (__ldcg(&recs[c].err)) s_bad = 1;
-        __syncthreads();
-        timeout = s_bad != 0;
-        __syncthreads();
+    const int tid = threadIdx.x, x = blockIdx.x;
+    constexpr int kReqs = 4;              // requests checked before the wait (any further ones after it)
+    int st_pre[kReqs];
+#pragma unroll
+    for (int k = 0; k < kReqs; ++k) {
+        const int b = x + k * (int)gridDim.x;
+        st_pre[k] = b < a.B ? request_status(a, b, &s_flag) : SV_OK;
     }
+    pdl_wait_prior();   // the attention grid has completed and its results are visible from here on
 
-    // 1. statuses, and zero outputs of failed requests
-    for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
-        if (tid == 0) s_bad = 0;
-        __syncthreads();
-        const int L = __ldg(a.kv_len + b);
-        if (tid < T) {
-            const int p = __ldg(a.parent + (size_t)b * T + tid);
-            if (tid == 0 ? p != -1 : (p < 0 || p >= tid)) s_bad = 1;
-        }
-        __syncthreads();
-        int st = s_bad ? SV_ERR_BAD_TREE : SV_OK;
-        if (st == SV_OK && (L < 0 || L + T > a.kv_cap)) st = SV_ERR_INVALID_ARG;
-        if (st == SV_OK && a.page_table) {   // every page the request reads must name a page of the pool
-            __syncthreads();
-            if (tid == 0) s_bad = 0;
-            __syncthreads();
-            const int32_t* pt = a.page_table + (size_t)b * a.max_pages;
-            for (int i = tid; i <= (L + T - 1) >> a.page_shift; i += blockDim.x)
-                if (__ldg(pt + i) < 0 || __ldg(pt + i) >= a.num_pages) s_bad = 1;
-            __syncthreads();
-            if (s_bad) st = SV_ERR_INVALID_ARG;
-        }
-        if (timeout) st = SV_ERR_TIMEOUT;
+    // the records (L2: written by the attention grid), with the time-out flags
+    const SplitRec* recs = (const SplitRec*)((const uint8_t*)a.ws + rec_off());
+    if (tid == 0) s_to = 0;
+    int chunks = 0;
+    if (tid < grid_main) {
+        const int4 r0 = __ldcg((const int4*)(recs + tid)), r1 = __ldcg((const int4*)(recs + tid) + 1);
+        SplitRec r;
+        r.unit = r0.x; r.b = r0.y; r.hk = r0.z; r.row0 = r0.w;
+        r.rows = r1.x; r.cf = r1.y; r.cf_slot = r1.z; r.err = r1.w;
+        s_rec[tid] = r;
+        chunks = r.unit >= 0 ? (r.rows + kMergeRows - 1) / kMergeRows : 0;
+    }
+    __syncthreads();
+    if (tid < grid_main && s_rec[tid].err) s_to = 1;
+    long long total;
+    const int pfx = (int)block_scan(chunks, s_scan, &total);   // ends with __syncthreads
+    if (tid < grid_main) s_pfx[tid] = pfx;
+    if (tid == 0) s_pfx[grid_main] = (int)total;
+    __syncthreads();
+
+    // statuses (after a time-out every status says so: the outputs are garbage then)
+    for (int k = 0, b = x; b < a.B; ++k, b += gridDim.x) {
+        int st = k < kReqs ? st_pre[k] : request_status(a, b, &s_flag);
+        if (s_to) st = SV_ERR_TIMEOUT;
         if (tid == 0 && a.status) a.status[b] = st;
         if (st != SV_OK && st != SV_ERR_TIMEOUT) {
             const size_t n = (size_t)T * a.Hq;
@@ -1107,87 +1131,75 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const __grid_
             for (size_t i = tid; i < n * kD / 8; i += blockDim.x) ((uint4*)o)[i] = make_uint4(0, 0, 0, 0);
             if (a.lse) for (size_t i = tid; i < n; i += blockDim.x) a.lse[(size_t)b * n + i] = 0.f;
         }
-        __syncthreads();
     }
-    // 2. merges
+
+    // merges (a request that fails its checks keeps the zero outputs of its status CTA: the record of a malformed
+    // tree names no unit, and a bad page table is checked here)
     const uint8_t* slots = (const uint8_t*)a.ws + slots_off();
-    for (int u = blockIdx.x; u < grid_main * kMergeUnits; u += gridDim.x) {
-        const int cl = u / kMergeUnits, rb = u - cl * kMergeUnits;
-        const SplitRec rec = recs[cl];
-        if (rec.unit < 0 || rec.rows <= rb * kMergeRows) continue;
-        // a request that fails validation keeps the zero outputs of step 1 (checked here again: step 1 may run in
-        // another CTA, before or after this one)
-        if (tid == 0) s_bad = 0;
-        __syncthreads();
-        {
-            const int L = __ldg(a.kv_len + rec.b);
-            if (tid < T) {
-                const int p = __ldg(a.parent + (size_t)rec.b * T + tid);
-                if (tid == 0 ? p != -1 : (p < 0 || p >= tid)) s_bad = 1;
-            }
-            if (L < 0 || L + T > a.kv_cap) s_bad = 1;
-            else if (a.page_table) {
-                const int32_t* pt = a.page_table + (size_t)rec.b * a.max_pages;
-                for (int i = tid; i <= (L + T - 1) >> a.page_shift; i += blockDim.x)
-                    if (__ldg(pt + i) < 0 || __ldg(pt + i) >= a.num_pages) s_bad = 1;
-            }
+    for (int task = x; task < (int)total; task += gridDim.x) {
+        int lo = 0, hi = grid_main - 1;   // the record holding chunk `task`: the last c with s_pfx[c] <= task
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_pfx[mid] <= task) lo = mid;
+            else hi = mid - 1;
         }
-        __syncthreads();
-        if (s_bad) continue;
-        float m[2][4], l[2][4];
-        uint2 x[2][4];
-        int rr[2];
-        // contributors are CTAs cf, cf + 1, ..., cl; CTA c > cf holds the unit in its first slot 2c
-        for (int h = 0; h < 2; ++h) rr[h] = rb * kMergeRows + warp * 2 + h;
-        float M[2] = {-INFINITY, -INFINITY}, Ls[2] = {0.f, 0.f}, acc[2][4] = {};
-        for (int c0 = rec.cf; c0 <= cl; c0 += 4) {
+        const int ci = lo;
+        const SplitRec rec = s_rec[ci];
+        const int chunk = task - s_pfx[ci];
+        if (a.page_table) {
+            if (request_status(a, rec.b, &s_flag) != SV_OK) continue;
+        }
+        const int r = chunk * kMergeRows + (tid >> 3), d0 = (tid & 7) * 16;
+        const int rr = min(r, rec.rows - 1);
+        float M = -INFINITY, Ls = 0.f, acc[16];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+        for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+        for (int c0 = rec.cf; c0 <= ci; c0 += kMergeBatch) {
+            float m[kMergeBatch], l[kMergeBatch];
+            uint4 v[kMergeBatch][2];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int c = min(c0 + i, cl);
-                    const int sidx = c == rec.cf ? rec.cf_slot : 2 * c;
-                    const uint8_t* base = slots + (long long)sidx * slot_bytes();
-                    const int r = min(rr[h], rec.rows - 1);
-                    const float* ml = (const float*)(base + (size_t)kUnitRows * kD * 2);
-                    m[h][i] = c0 + i <= cl ? __ldcg(ml + r) : -INFINITY;
-                    l[h][i] = __ldcg(ml + kUnitRows + r);
-                    x[h][i] = __ldcg((const uint2*)((const uint16_t*)base + (size_t)r * kD) + lane);
+            for (int i = 0; i < kMergeBatch; ++i) {
+                const int c = min(c0 + i, ci);
+                const uint8_t* base = slots + (long long)(c == rec.cf ? rec.cf_slot : 2 * c) * slot_bytes();
+                const float* ml = (const float*)(base + (size_t)kUnitRows * kD * 2);
+                m[i] = c0 + i <= ci ? __ldcg(ml + rr) : -INFINITY;
+                l[i] = __ldcg(ml + kUnitRows + rr);
+                const uint4* src = (const uint4*)((const uint16_t*)base + (size_t)rr * kD + d0);
+                v[i][0] = __ldcg(src);
+                v[i][1] = __ldcg(src + 1);
+            }
+            float mn = M;
+#pragma unroll
+            for (int i = 0; i < kMergeBatch; ++i) mn = fmaxf(mn, m[i]);
+            const float sc = M == -INFINITY ? 0.f : ex2(M - mn);   // rescale the running sums
+            Ls *= sc;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) acc[e] *= sc;
+#pragma unroll
+            for (int i = 0; i < kMergeBatch; ++i) {
+                // a partial that saw no finite score (or a padding contributor) weighs nothing
+                const float w = m[i] == -INFINITY ? 0.f : l[i] * ex2(m[i] - mn);
+                Ls += w;
+                const uint32_t wv[8] = {v[i][0].x, v[i][0].y, v[i][0].z, v[i][0].w,
+                                        v[i][1].x, v[i][1].y, v[i][1].z, v[i][1].w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    acc[2 * e] += __uint_as_float(wv[e] << 16) * w;
+                    acc[2 * e + 1] += __uint_as_float(wv[e] & 0xffff0000u) * w;
                 }
             }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                float mn = M[h];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) mn = fmaxf(mn, m[h][i]);
-                const float sc = M[h] == -INFINITY ? 0.f : ex2(M[h] - mn);   // rescale the running sums
-                Ls[h] *= sc;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[h][e] *= sc;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float w = m[h][i] == -INFINITY ? 0.f : l[h][i] * ex2(m[h][i] - mn);
-                    Ls[h] += w;
-                    acc[h][0] += __uint_as_float(x[h][i].x << 16) * w;
-                    acc[h][1] += __uint_as_float(x[h][i].x & 0xffff0000u) * w;
-                    acc[h][2] += __uint_as_float(x[h][i].y << 16) * w;
-                    acc[h][3] += __uint_as_float(x[h][i].y & 0xffff0000u) * w;
-                }
-                M[h] = mn;
-            }
+            M = mn;
         }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int r = rr[h];
-            if (r >= rec.rows) continue;
+        if (r < rec.rows) {
             const int qi = rec.row0 + r, t_node = qi / G, g_head = qi - t_node * G;
             const size_t out_row = ((size_t)rec.b * T + t_node) * a.Hq + (size_t)rec.hk * G + g_head;
-            const float inv = Ls[h] > 0.f ? 1.f / Ls[h] : 0.f;
-            const __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[h][0] * inv, acc[h][1] * inv);
-            const __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[h][2] * inv, acc[h][3] * inv);
-            ((uint2*)((uint16_t*)a.out + out_row * kD))[lane] =
-                make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1));
-            if (a.lse && lane == 0) a.lse[out_row] = (M[h] + __log2f(Ls[h])) * 0.69314718055994531f;
+            const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+            uint4* dst = (uint4*)((uint16_t*)a.out + out_row * kD + d0);
+            dst[0] = make_uint4(pack2<false>(acc[0] * inv, acc[1] * inv), pack2<false>(acc[2] * inv, acc[3] * inv),
+                                pack2<false>(acc[4] * inv, acc[5] * inv), pack2<false>(acc[6] * inv, acc[7] * inv));
+            dst[1] = make_uint4(pack2<false>(acc[8] * inv, acc[9] * inv), pack2<false>(acc[10] * inv, acc[11] * inv),
+                                pack2<false>(acc[12] * inv, acc[13] * inv), pack2<false>(acc[14] * inv, acc[15] * inv));
+            if (a.lse && (tid & 7) == 0) a.lse[out_row] = (M + __log2f(Ls)) * 0.69314718055994531f;
         }
     }
 }
@@ -1252,6 +1264,19 @@ long long view_rows(const AttnArgs& a) {
 
 // CTAs that fit on the device at once with this kernel's resources (cached per kernel); the persistent grid
 // never exceeds it, so every CTA of the grid is resident from the start.
+// merge CTAs resident at once (the merge grid never waits for a second wave)
+int merge_ctas() {
+    static int n = 0;
+    if (!n) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_merge_kernel, kMergeThreads, 0) != cudaSuccess ||
+            per_sm < 1)
+            per_sm = 1;
+        n = per_sm * num_sms();
+    }
+    return n;
+}
+
 template <int KVK, int KS>
 int resident_ctas() {
     static int n = 0;
@@ -1346,7 +1371,7 @@ cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t s) {
     default: e = launch_kind<KV_BF16>(a, s, sl2, &grid); break;
     }
     if (e != cudaSuccess) return e;
-    return launch_ex(attn_merge_kernel, dim3(grid * kMergeUnits), dim3(kMergeThreads), 0, s, 1, true, a, grid);
+    return launch_ex(attn_merge_kernel, dim3(merge_ctas()), dim3(kMergeThreads), 0, s, 1, true, a, grid);
 }
 
 }  // namespace sv

@@ -7,7 +7,7 @@ import pytest
 
 import oracle
 from speculative_decoding_tree_verify_gb300 import workloads as W
-from tests.gpu_util import run_attn
+from tests.gpu_util import dev, host_f32, run_attn
 
 pytestmark = pytest.mark.gpu
 
@@ -56,8 +56,9 @@ SMALL = [
     (2, 1, 8, 1, 128, (1, 1000), "chain", "bf16", "bf16"),
     (2, 20, 4, 2, 64, (31, 33), "star", "f32", "bf16"),
     (2, 7, 6, 3, 96, (50, 90), (2, 2, 1), "bf16", "bf16"),
-    # tensor-core path with Q loaded by the 3D TMA box (G = 1, G = 16 over 2-CTA clusters), and with Q written
-    # by the softmax warps because G does not divide the 128-row M tile (G = 3; G = 6 over 2-CTA clusters)
+    # tensor-core path with Q loaded by the 3D TMA box (G = 1 in split mode, G = 16 with 320 rows per kv
+    # head: a pair unit and a split-mode unit), and with Q written by the softmax warps because G does not divide the
+    # 128-row M tile (G = 3 in split mode; G = 6 in pair mode)
     (2, 40, 4, 4, 128, (70, 400), (4, 3, 2), "bf16", "bf16"),
     (2, 20, 32, 2, 128, (64, 300), (4, 2, 2), "bf16", "bf16"),
     (2, 11, 9, 3, 128, (90, 400), (3, 2, 2), "bf16", "bf16"),
@@ -157,3 +158,49 @@ def test_fp8_long_context_full_batch_sampled_rows():
     err = np.abs(out[b, i, hh] - ref_o[j, i, hh]).max()
     assert err <= 6e-2, err
     assert np.abs(lse[b, i, hh] - ref_l[j, i, hh]).max() <= 1e-3
+
+
+def test_attn_workspace_any_content_and_reuse():
+    # The partial results of units that cross CTA range boundaries, and the records the merge kernel reads, live
+    # in the workspace: a workspace of arbitrary bytes works on its first call, and reusing it, with calls of
+    # another shape in between, gives bit-identical results.  Short prefixes make almost every unit span several
+    # CTAs.
+    import torch
+    from speculative_decoding_tree_verify_gb300 import sv
+
+    def call(w, ws):
+        q, k, v = dev(w.q), dev(w.k), dev(w.v)
+        out = torch.empty_like(q)
+        lse = torch.empty((w.B, w.T, w.Hq), dtype=torch.float32, device="cuda")
+        st = torch.full((w.B,), -7, dtype=torch.int32, device="cuda")
+        sv.tree_attn(q, k, v, dev(w.kv_len), dev(w.parent), out, lse=lse, status=st, workspace=ws)
+        torch.cuda.synchronize()
+        return host_f32(out, w.q_dt), lse.cpu().numpy(), st.cpu().numpy()
+
+    w1 = W.make_verify(11, B=4, T=60, Hq=32, Hkv=8, D=128, L=(300, 1500), V=64, q_dt="bf16", kv_dt="bf16",
+                       tree=(4, 3, 2, 2, 1, 1))
+    w2 = W.make_verify(12, B=5, T=13, Hq=8, Hkv=2, D=128, L=(100, 900), V=64, q_dt="bf16", kv_dt="bf16",
+                       tree=(3, 2, 2))
+    n = max(sv.workspace_size(sv.OP_TREE_ATTN, w.B, w.T, w.Hq, w.Hkv, w.D, w.kv_cap, 0) for w in (w1, w2))
+    g = torch.Generator(device="cuda").manual_seed(5)
+    ref = {}
+    for w in (w1, w2):
+        o, l, s, _ = oracle.tree_attn_w(w)
+        ref[id(w)] = (o, l, s)
+    for fill in ("random", "ones", "zeros"):
+        if fill == "random":
+            ws = torch.randint(0, 256, (n,), dtype=torch.uint8, device="cuda", generator=g)
+        else:
+            ws = torch.full((n,), 255 if fill == "ones" else 0, dtype=torch.uint8, device="cuda")
+        first = {}
+        for rep in range(3):
+            for w in (w1, w2):
+                out, lse, st = call(w, ws)
+                o, l, s = ref[id(w)]
+                np.testing.assert_array_equal(st, s)
+                assert np.abs(out - o).max() <= 2e-2, (fill, rep)
+                assert np.abs(lse - l).max() <= 1e-3, (fill, rep)
+                if rep == 0:
+                    first[id(w)] = (out, lse)
+                else:
+                    assert np.array_equal(out, first[id(w)][0]) and np.array_equal(lse, first[id(w)][1])
