@@ -354,7 +354,7 @@ struct SoftmaxState {
 struct MainShared {
     uint64_t full[5], raw[5], empty[5];                    // K slots 0 .. KS-1 and V slots 3, 4
     uint64_t s_full[2], p_full[2], o_full[2];              // per side
-    uint64_t o_free;                                       // the segment's O has been read by both sides
+    uint64_t o_free[2][2];                                 // [O_A / O_B][dims 0..63 / 64..127] read by the epilogue
     uint64_t q_full, q_ready, q_empty, drain[2];
     uint64_t conv_bar;                                     // e2m1 caches: the converters have read the raw tile
     float ml[2][2][kRows];                                 // split-mode epilogue: [side][m][row]
@@ -400,7 +400,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             mbar_init(&sh.o_full[s], 1);
             mbar_init(&sh.drain[s], 1);
         }
-        mbar_init(&sh.o_free, 8);
+        for (int x = 0; x < 4; ++x) mbar_init(&sh.o_free[x >> 1][x & 1], 4);   // the four warps that read it
         mbar_init(&sh.q_full, q_tma ? 1 : 8);        // the TMA transaction, or the eight softmax warps
         mbar_init(&sh.q_ready, 4);                   // the converters rounded Q to f16 (8-bit / 4-bit caches)
         mbar_init(&sh.q_empty, 1);
@@ -411,6 +411,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmQ);
     }
     if (warp == 1) tmem_alloc(&sh.tmem, 512);
     make_plan(a, UQ, blockIdx.x, gridDim.x, &sh.plan, sh.scan);   // ends with __syncthreads
@@ -450,6 +451,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                         uint8_t* qdst = smem + kSmemQ + m * kSlotBytes;
                         tma_load_3d(qdst, &tmQ, 0, sg.hk * G, sg.b * T + t0, &sh.q_full);
                         tma_load_3d(qdst + kBoxBytes, &tmQ, 64, sg.hk * G, sg.b * T + t0, &sh.q_full);
+                    }
+                    // the next segment's Q into L2 now: its load, once this Q is released, then comes from L2
+                    SegIter pi = si;
+                    Seg ps;
+                    if (pi.next(ps)) {
+                        for (int m = 0; m < (ps.pair ? 2 : 1); ++m) {
+                            const int t0 = (ps.qg * kUnitRows + m * kRows) / G;
+                            tma_prefetch_3d(&tmQ, 0, ps.hk * G, ps.b * T + t0);
+                            tma_prefetch_3d(&tmQ, 64, ps.hk * G, ps.b * T + t0);
+                        }
                     }
                 }
                 ++nseg;
@@ -507,6 +518,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             SegIter si;
             si.init(a, plan, UQ, QG, TG);
             Seg sg;
+            // S MMAs of the segment still to issue.  When every unit is in split mode (the 3-slot K ring), a segment
+            // releases its Q tile after the last of them; otherwise Q is released with the segment's O (the next Q
+            // then loads in the switch's bubble, not under the last tile's MMAs, which measured faster).
+            int s_left = 0;
             // S_X = Q_X K(tile)^T; commit to s_full_X (and release the K slot when `release`)
             // (split mode: both sides multiply Q tile A)
             auto issue_s = [&](int side, uint32_t ridx, bool release, bool pair) -> bool {
@@ -520,19 +535,33 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                                at(dK, kb + (kk >> 2) * kBoxBytes + (kk & 3) * 32), idS, kk > 0);
                 mma_commit(&sh.s_full[side]);
                 if (release) mma_commit(&sh.empty[slot]);
+                if constexpr (KS == 3)
+                    if (--s_left == 0) mma_commit(&sh.q_empty);   // Q may be overwritten once these complete
                 return true;
             };
-            // O_X += P_X V(tile) (P in the side's S columns); release the V slot when `release`
-            auto issue_pv = [&](int side, uint32_t ridx, bool first, bool release) -> bool {
+            // O_X += P_X V(tile) (P in the side's S columns); release the V slot when `release`.  The first PV of a
+            // segment after the first (`o_wait`) overwrites O_X once the previous segment's epilogue has read both
+            // halves of it.
+            auto issue_pv = [&](int side, uint32_t ridx, bool first, bool release, bool o_wait) -> bool {
                 const uint32_t slot = ridx & 1;
                 if (!mbar_wait(&sh.full[kVBar + slot], (ridx >> 1) & 1, err, a.wait_cycles)) return false;
                 if (!mbar_wait(&sh.p_full[side], g[side] & 1, err, a.wait_cycles)) return false;
                 tc_fence_after();
                 const uint32_t vb = sV + slot * kSlotBytes;
+                if (!o_wait) {
 #pragma unroll
-                for (int kk = 0; kk < kTileN / 16; ++kk)
-                    mma_f16_ts(tmem + col_O(side), tmem + col_S(side) + kk * 8, at(dV, vb + kk * 2048), idO,
-                               (!first || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kTileN / 16; ++kk)
+                        mma_f16_ts(tmem + col_O(side), tmem + col_S(side) + kk * 8, at(dV, vb + kk * 2048), idO,
+                                   (!first || kk > 0) ? 1u : 0u);
+                } else {
+                    for (int h = 0; h < 2; ++h)
+                        if (!mbar_wait(&sh.o_free[side][h], (nseg - 1) & 1, err, a.wait_cycles)) return false;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kTileN / 16; ++kk)
+                        mma_f16_ts(tmem + col_O(side), tmem + col_S(side) + kk * 8, at(dV, vb + kk * 2048), idO,
+                                   (!first || kk > 0) ? 1u : 0u);
+                }
                 if (release) mma_commit(&sh.empty[kVBar + slot]);
                 ++g[side];
                 return true;
@@ -540,33 +569,27 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             while (ok && !*err && si.next(sg)) {
                 const int nt = sg.t1 - sg.t0;
                 const int n0 = side_tiles(sg.pair, nt, 0), n1 = side_tiles(sg.pair, nt, 1);
+                s_left = n0 + n1;
                 ok = mbar_wait(qbar_ready ? &sh.q_ready : &sh.q_full, nseg & 1, err, a.wait_cycles);
                 if (!ok) break;
                 tc_fence_after();
                 const bool rel0 = !sg.pair;                // pair mode: side B is a tile's last reader
                 if (n0 > 0) ok = issue_s(0, base + side_tile(sg.pair, 0, 0), rel0, sg.pair);
                 if (ok && n1 > 0) ok = issue_s(1, base + side_tile(sg.pair, 0, 1), true, sg.pair);
-                bool o_waited = nseg == 0;
                 const int nmax = n0 > n1 ? n0 : n1;
                 for (int i = 0; i < nmax && ok; ++i) {
                     for (int side = 0; side < 2 && ok; ++side) {
                         const int ns = side ? n1 : n0;
                         if (i >= ns) continue;
-                        if (!o_waited) {   // the previous segment's epilogue has read O_A and O_B
-                            ok = mbar_wait(&sh.o_free, (nseg - 1) & 1, err, a.wait_cycles);
-                            if (!ok) break;
-                            tc_fence_after();
-                            o_waited = true;
-                        }
                         const bool rel = side == 1 || !sg.pair;
-                        ok = issue_pv(side, base + side_tile(sg.pair, i, side), i == 0, rel);
+                        ok = issue_pv(side, base + side_tile(sg.pair, i, side), i == 0, rel, i == 0 && nseg > 0);
                         if (ok && i + 1 < ns) ok = issue_s(side, base + side_tile(sg.pair, i + 1, side), rel, sg.pair);
                     }
                 }
                 if (!ok) break;
                 mma_commit(&sh.o_full[0]);
                 mma_commit(&sh.o_full[1]);
-                mma_commit(&sh.q_empty);   // after the segment's last S MMA
+                if constexpr (KS != 3) mma_commit(&sh.q_empty);
                 base += (uint32_t)nt;
                 ++nseg;
             }
@@ -765,61 +788,74 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 all_sync();   // sh.ml / sh.pl may be rewritten only after both sides read them
             }
             if (wait(&sh.o_full[0], ss.pend_nseg & 1) && wait(&sh.o_full[1], ss.pend_nseg & 1)) tc_fence_after();
-            if (!dead) {
-                const float inv = Lsum > 0.f ? osc / Lsum : 0.f;
-                uint8_t* part = pg.split ? (uint8_t*)a.ws + slots_off() + (long long)pg.slot * slot_bytes() : nullptr;
-                // pair mode: this side's whole row (d 0..127); split mode: side A d 0..63, side B d 64..127
-                const int d0 = pr ? 0 : 64 * side, nch = pr ? 8 : 4;
-                uint16_t* dst_row = part ? (uint16_t*)part + (size_t)urow * kD : (uint16_t*)a.out + out_row * kD;
+            // O is read 16 columns at a time, normalised to bf16 pairs and stored; each 64-column half is released
+            // (o_free) as soon as it has been read.
+            // Pair mode: this side reads its own O, both halves; split mode: side A reads dims 0..63 of O_A and O_B,
+            // side B dims 64..127.
+            const float inv = Lsum > 0.f ? osc / Lsum : 0.f;
+            uint8_t* part = pg.split ? (uint8_t*)a.ws + slots_off() + (long long)pg.slot * slot_bytes() : nullptr;
+            uint16_t* dst_row = part ? (uint16_t*)part + (size_t)urow * kD : (uint16_t*)a.out + out_row * kD;
 #pragma unroll 1
-                for (int c = 0; c < nch; ++c) {   // 16 columns at a time
-                    uint32_t oa[16], ob[16];
-                    __syncwarp();
-                    tmem_ld16(tmem + lane_addr + col_O(pr ? side : 0) + d0 + 16 * c, oa);
-                    if (!pr) tmem_ld16(tmem + lane_addr + col_O(1) + d0 + 16 * c, ob);
-                    tmem_ld_wait();
-                    reg_fence(oa);
-                    if (!pr) reg_fence(ob);
-                    if (valid) {
-                        uint4* dst = (uint4*)(dst_row + d0 + 16 * c);
+            for (int h = 0; h < 2; ++h) {
+                if (!pr && h != side) continue;
+                if (!dead) {
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {   // 16 columns at a time
+                        uint32_t oa[16], ob[16];
+                        __syncwarp();
+                        tmem_ld16(tmem + lane_addr + col_O(pr ? side : 0) + 64 * h + 16 * c, oa);
+                        if (!pr) tmem_ld16(tmem + lane_addr + col_O(1) + 64 * h + 16 * c, ob);
+                        tmem_ld_wait();
+                        reg_fence(oa);
+                        if (!pr) reg_fence(ob);
+                        uint32_t pk[8];
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            uint32_t v[4];
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                // a side that saw no finite score (weight 0) contributes exactly nothing
-                                float x0 = wa > 0.f ? __uint_as_float(oa[8 * e + 2 * q]) * wa : 0.f;
-                                float x1 = wa > 0.f ? __uint_as_float(oa[8 * e + 2 * q + 1]) * wa : 0.f;
-                                if (!pr && wb > 0.f) {
-                                    x0 += __uint_as_float(ob[8 * e + 2 * q]) * wb;
-                                    x1 += __uint_as_float(ob[8 * e + 2 * q + 1]) * wb;
-                                }
-                                v[q] = pack2<false>(x0 * inv, x1 * inv);
+                        for (int q = 0; q < 8; ++q) {
+                            // a side that saw no finite score (weight 0) contributes exactly nothing
+                            float x0 = wa > 0.f ? __uint_as_float(oa[2 * q]) * wa : 0.f;
+                            float x1 = wa > 0.f ? __uint_as_float(oa[2 * q + 1]) * wa : 0.f;
+                            if (!pr && wb > 0.f) {
+                                x0 += __uint_as_float(ob[2 * q]) * wb;
+                                x1 += __uint_as_float(ob[2 * q + 1]) * wb;
                             }
-                            dst[e] = make_uint4(v[0], v[1], v[2], v[3]);
+                            pk[q] = pack2<false>(x0 * inv, x1 * inv);
+                        }
+                        if (valid) {
+                            uint4* dst = (uint4*)(dst_row + 64 * h + 16 * c);
+                            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
                         }
                     }
-                }
-                if (valid && (pr || side == 0)) {
-                    if (part) {
-                        float* ml = (float*)(part + (size_t)kUnitRows * kD * 2);
-                        ml[urow] = M;
-                        ml[kUnitRows + urow] = Lsum;
-                    } else if (a.lse) {
-                        a.lse[out_row] = (M + __log2f(Lsum)) * 0.69314718055994531f;
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&sh.o_free[pr ? side : 0][h]);
+                        if (!pr) mbar_arrive(&sh.o_free[1][h]);
+                    }
+                } else {
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&sh.o_free[pr ? side : 0][h]);
+                        if (!pr) mbar_arrive(&sh.o_free[1][h]);
                     }
                 }
-                tc_fence_before();
+            }
+            if (!dead && valid && (pr || side == 0)) {
+                if (part) {
+                    float* ml = (float*)(part + (size_t)kUnitRows * kD * 2);
+                    ml[urow] = M;
+                    ml[kUnitRows + urow] = Lsum;
+                } else if (a.lse) {
+                    a.lse[out_row] = (M + __log2f(Lsum)) * 0.69314718055994531f;
+                }
             }
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&sh.o_free);
-                ss.pend_on = 0;
-            }
+            if (lane == 0) ss.pend_on = 0;
             __syncwarp();
         };
 
         bool first_seg = true;
+        int par_b = -1;   // the request whose parent array sh.par holds
         for (;;) {
             if (lane == 0) ss.has = ss.it.next(ss.seg) ? 1 : 0;
             __syncwarp();
@@ -862,18 +898,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             }
 
             // ancestors of this row's node from the request's parent array (walk bounded by T, so a malformed
-            // array cannot trap; such requests are zeroed and flagged by the merge kernel)
-            all_sync();
+            // array cannot trap; such requests are zeroed and flagged by the merge kernel); the array is loaded
+            // when the segment's request differs from the previous segment's
             int bad = 0;   // this node's parent breaks the tree's topological order
-            if (side == 0 && row < T) {
-                const int px = __ldg(a.parent + (size_t)b * T + row);
-                sh.par[row] = px;
-                bad = row == 0 ? px != -1 : (px < 0 || px >= row);
+            if (b != par_b) {
+                all_sync();   // every warp has walked the previous request's array
+                if (side == 0 && row < T) {
+                    const int px = __ldg(a.parent + (size_t)b * T + row);
+                    sh.par[row] = px;
+                    bad = row == 0 ? px != -1 : (px < 0 || px >= row);
+                }
+                // the barrier also ORs the flags: bad != 0 everywhere if any node's parent is out of order
+                asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbar.red.or.pred q, 1, 256, p;\n\t"
+                             "selp.s32 %0, 1, 0, q;\n\t}"
+                             : "=r"(bad) : "r"(bad) : "memory");
+                par_b = b;
             }
-            // the barrier also ORs the flags: bad != 0 everywhere if any node's parent is out of order
-            asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbar.red.or.pred q, 1, 256, p;\n\t"
-                         "selp.s32 %0, 1, 0, q;\n\t}"
-                         : "=r"(bad) : "r"(bad) : "memory");
             if (side == 0 && row == 0 && first_seg) {
                 // the unit that began in an earlier CTA's range and ends in this one is merged by attn_merge_kernel
                 const Seg& sg = ss.seg;
