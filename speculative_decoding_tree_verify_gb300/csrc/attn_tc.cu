@@ -962,17 +962,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                     const uint32_t tree = a0 >= 64 ? 0u : a0 >= 0 ? (uint32_t)(anc >> a0) : a0 > -32 ? (uint32_t)(anc << -a0) : 0u;
                     return valid_row ? (pre | tree) : 0u;
                 };
-                // pass 1: the row's max over the tile, 32 columns per TMEM load (tiles inside the prefix take the
-                // variant without the mask)
+                // pass 1: the row's max over the tile, two 32-column TMEM loads in flight at a time (tiles inside the
+                // prefix take the variant without the mask)
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
                 auto pass1 = [&](auto mask_tag) {
                     constexpr bool MASK = decltype(mask_tag)::value;
-#pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(tS + 32 * c, r);
-                        tmem_ld_wait();
-                        reg_fence(r);
+                    auto fold = [&](const uint32_t (&r)[32], int c) {
                         const uint32_t al = MASK ? allow_word(c) : ~0u;
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
@@ -984,6 +979,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                             }
                             mx[q] = max3(mx[q], max3(v[0], v[1], v[2]), max3(max3(v[3], v[4], v[5]), v[6], v[7]));
                         }
+                    };
+#pragma unroll 1
+                    for (int c = 0; c < 4; c += 2) {
+                        uint32_t r0[32], r1[32];
+                        tmem_ld32(tS + 32 * c, r0);
+                        tmem_ld32(tS + 32 * c + 32, r1);
+                        tmem_ld_wait();
+                        reg_fence(r0);
+                        reg_fence(r1);
+                        fold(r0, c);
+                        fold(r1, c + 1);
                     }
                 };
                 if (masked) pass1(std::true_type{});
