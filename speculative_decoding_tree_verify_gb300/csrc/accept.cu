@@ -935,7 +935,13 @@ cudaError_t launch_typed(const AcceptArgs& a, cudaStream_t s) {
     } else if (stoch) e = launch_ex(accept_rows_kernel<LDT, true>, dim3(CL * rows), dim3(kRowThreads), 0, s, CL, false, a, CL, chunk, rows_src);
     else       e = launch_ex(accept_rows_kernel<LDT, false>, dim3(CL * rows), dim3(kRowThreads), 0, s, CL, false, a, CL, chunk, rows_src);
     if (e != cudaSuccess) return e;
-    const int CLW = (mode == MODE_GREEDY) ? 1 : pick_cluster(a.V, kWalkThreads * 8);
+    // walk clusters: enough CTAs per request for the residual passes, but no more than the walk kernel keeps
+    // resident at once over all requests (a second wave would repeat each request's serial chain of steps)
+    int CLW = 1;
+    if (mode != MODE_GREEDY) {
+        const int cap = pick_cluster(a.V, kWalkThreads * 8);
+        while (CLW * 2 <= cap && (long long)a.B * CLW * 2 <= 2LL * sm_count()) CLW *= 2;
+    }
     switch (mode) {
     case MODE_GREEDY: return launch_ex(accept_walk_kernel<LDT, MODE_GREEDY>, dim3(a.B), dim3(kWalkThreads), 0, s, 1, true, a, 1);
     case MODE_PROB:   return launch_ex(accept_walk_kernel<LDT, MODE_PROB>, dim3(a.B * CLW), dim3(kWalkThreads), 0, s, CLW, true, a, CLW);
