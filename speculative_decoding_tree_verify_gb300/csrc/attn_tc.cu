@@ -452,16 +452,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                         tma_load_3d(qdst, &tmQ, 0, sg.hk * G, sg.b * T + t0, &sh.q_full);
                         tma_load_3d(qdst + kBoxBytes, &tmQ, 64, sg.hk * G, sg.b * T + t0, &sh.q_full);
                     }
-                    // the next segment's Q into L2 now: its load, once this Q is released, then comes from L2
-                    SegIter pi = si;
-                    Seg ps;
-                    if (pi.next(ps)) {
-                        for (int m = 0; m < (ps.pair ? 2 : 1); ++m) {
-                            const int t0 = (ps.qg * kUnitRows + m * kRows) / G;
-                            tma_prefetch_3d(&tmQ, 0, ps.hk * G, ps.b * T + t0);
-                            tma_prefetch_3d(&tmQ, 64, ps.hk * G, ps.b * T + t0);
-                        }
-                    }
                 }
                 ++nseg;
                 for (int t = sg.t0; t < sg.t1 && !*err; ++t, ++n) {

@@ -105,13 +105,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int32_t
         : "memory");
 }
 
-// 3D box prefetch into L2 (no shared memory, no barrier; same coordinate rules as the load).
-__device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int32_t x, int32_t y, int32_t z) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];"
-                 ::"l"((uint64_t)tmap), "r"(x), "r"(y), "r"(z)
-                 : "memory");
-}
-
 // ------------------------------------------------------------------------------------------------ cluster
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
