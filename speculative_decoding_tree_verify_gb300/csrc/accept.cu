@@ -448,7 +448,8 @@ __global__ void __launch_bounds__(kStoThreads) accept_rows_staged_kernel(AcceptA
         zmin = fminf(zmin, *cluster.map_shared_rank(&s_zmin, q));
         err |= *cluster.map_shared_rank(&s_err, q);
     }
-    cluster.sync();   // partials consumed
+    // (no barrier here: s_zmax / s_zmin / s_err are not written again, and no CTA leaves before the barriers
+    // below, so the remote reads above stay valid)
 
     // every z finite iff max and min are; every y finite iff the two extremes of y are (y monotone in z)
     const float invT = a.invT;
@@ -547,7 +548,9 @@ __global__ void __launch_bounds__(kStoThreads) accept_rows_staged_kernel(AcceptA
         int e2 = 0;
         for (int q = 0; q < kStoPieces; ++q) tc::mbar_wait(&s_bar[q], 0, &e2);
     }
-    cluster.sync();   // keep every CTA's shared memory alive until CTA 0 has read it
+    // keep every CTA's shared memory alive until CTA 0 has read it (CTA 0 has used the values it read before it
+    // arrives, so the barrier needs no memory ordering)
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
     pdl_launch_dependents();
 }
 
