@@ -387,6 +387,8 @@ __global__ void __launch_bounds__(kStoThreads) accept_rows_staged_kernel(AcceptA
 
     if (tid == 0) {
         s_err = 0;
+        s_S = 0;             // CTA 0's copies are the row's totals (every CTA adds after the first cluster barrier)
+        s_arg = 0x7fffffff;
         for (int q = 0; q < kStoPieces; ++q) tc::mbar_init(&s_bar[q], 1);
         tc::mbar_fence_init();
         for (int q = 0; q < kStoPieces; ++q) {
@@ -448,8 +450,8 @@ __global__ void __launch_bounds__(kStoThreads) accept_rows_staged_kernel(AcceptA
         zmin = fminf(zmin, *cluster.map_shared_rank(&s_zmin, q));
         err |= *cluster.map_shared_rank(&s_err, q);
     }
-    // (no barrier here: s_zmax / s_zmin / s_err are not written again, and no CTA leaves before the barriers
-    // below, so the remote reads above stay valid)
+    // (no barrier here: s_zmax / s_zmin / s_err are not written again, and no CTA leaves before the cluster barrier
+    // below, which every CTA reaches after these reads)
 
     // every z finite iff max and min are; every y finite iff the two extremes of y are (y monotone in z)
     const float invT = a.invT;
@@ -520,20 +522,17 @@ __global__ void __launch_bounds__(kStoThreads) accept_rows_staged_kernel(AcceptA
     if (lane == 0) { s_ws[warp] = S; s_redi[warp] = arg; }
     __syncthreads();
     if (tid == 0) {
+        // this CTA's sum and first argmax go into CTA 0's totals (atomics on distributed shared memory)
         u64 t = 0;
         int am = 0x7fffffff;
         for (int w = 0; w < kStoThreads / 32; ++w) { t += s_ws[w]; am = min(am, s_redi[w]); }
-        s_S = t;
-        s_arg = am;
+        atomicAdd(reinterpret_cast<unsigned long long*>(cluster.map_shared_rank(&s_S, 0)), (unsigned long long)t);
+        if (WANT_ARG) atomicMin(cluster.map_shared_rank(&s_arg, 0), am);
     }
-    cluster.sync();
+    cluster.sync();   // every CTA's share has reached CTA 0; nobody reads another CTA's shared memory after this
     if (rank == 0 && tid == 0) {
-        u64 t = 0;
-        int am = 0x7fffffff;
-        for (int q = 0; q < CL; ++q) {
-            t += *cluster.map_shared_rank(&s_S, q);
-            am = min(am, *cluster.map_shared_rank(&s_arg, q));
-        }
+        const u64 t = s_S;
+        const int am = s_arg;
         RowStat st;
         st.zmax = zmax;
         st.arg = (zfin && !err) ? am : -1;
@@ -548,9 +547,6 @@ __global__ void __launch_bounds__(kStoThreads) accept_rows_staged_kernel(AcceptA
         int e2 = 0;
         for (int q = 0; q < kStoPieces; ++q) tc::mbar_wait(&s_bar[q], 0, &e2);
     }
-    // keep every CTA's shared memory alive until CTA 0 has read it (CTA 0 has used the values it read before it
-    // arrives, so the barrier needs no memory ordering)
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
     pdl_launch_dependents();
 }
 
