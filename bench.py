@@ -331,41 +331,51 @@ def timed_graph_steps(graphs, steps, flush, stream, clock_index):
     return per_call, clk.summary()
 
 
-def e2e_time(host, dev_in, calls, outs_dev, steps, stream):
-    """Per-step time (ms) of: every input copied from pinned host memory (the large ones on their own streams),
-    the calls through the API, the outputs copied back to pinned host memory."""
+def e2e_time(host, dev_sets, call_sets, outs_dev, steps, stream):
+    """Per-step time (ms) through the API with every input copied from pinned host memory and the outputs
+    copied back, each step.  Two device copies of the inputs (`dev_sets`, with `call_sets` the calls bound to
+    each) let the next step's host-to-device copies, on their own stream, run while the current step computes;
+    a step's compute waits for its own copies, and a copy into a set waits until the step that last read it is
+    done.  The timed region spans the first step's copies to the last step's outputs."""
     import torch
     outs_host = {k: torch.empty(t.shape, dtype=t.dtype).pin_memory() for k, t in outs_dev.items()}
-    big = sorted(host, key=lambda k: -host[k].numel() * host[k].element_size())[:3]
-    side = {k: torch.cuda.Stream() for k in big}
+    copy_stream = torch.cuda.Stream()
+    copied = [torch.cuda.Event(), torch.cuda.Event()]
+    done = [torch.cuda.Event(), torch.cuda.Event()]
+    for e in done:
+        e.record(stream)
 
-    def one():
-        for k, t in host.items():
-            if k in side:
-                side[k].wait_stream(stream)
-                with torch.cuda.stream(side[k]):
-                    dev_in[k].copy_(t, non_blocking=True)
-            else:
-                dev_in[k].copy_(t, non_blocking=True)
-        for k in side:
-            stream.wait_stream(side[k])
-        for c in calls:
-            c()
-        for k, t in outs_host.items():
-            t.copy_(outs_dev[k], non_blocking=True)
+    def h2d(b):
+        copy_stream.wait_event(done[b])
+        with torch.cuda.stream(copy_stream):
+            for k, t in host.items():
+                dev_sets[b][k].copy_(t, non_blocking=True)
+            copied[b].record(copy_stream)
 
-    for _ in range(2):
-        one()
+    def run(n):
+        h2d(0)
+        for s in range(n):
+            b = s & 1
+            if s + 1 < n:
+                h2d(b ^ 1)
+            stream.wait_event(copied[b])
+            for c in call_sets[b]:
+                c()
+            for k, t in outs_host.items():
+                t.copy_(outs_dev[k], non_blocking=True)
+            done[b].record(stream)
+
+    run(2)
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for _ in range(steps):
-        one()
+    copy_stream.wait_stream(stream)
+    run(steps)
     t1.record(stream)
     torch.cuda.synchronize()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = sum(t.numel() * t.element_size() for t in outs_host.values())
-    return t0.elapsed_time(t1) / steps, h2d, d2h
+    h2d_bytes = sum(t.numel() * t.element_size() for t in host.values())
+    d2h_bytes = sum(t.numel() * t.element_size() for t in outs_host.values())
+    return t0.elapsed_time(t1) / steps, h2d_bytes, d2h_bytes
 
 
 # ------------------------------------------------------------------------------------------ the sv arm: verify
@@ -387,29 +397,34 @@ def run_sv_verify(args, w):
     ws_attn = torch.empty(max(sv.workspace_size(sv.OP_TREE_ATTN, B, T, w.Hq, w.Hkv, w.D, w.kv_cap, 0), 256),
                           dtype=torch.uint8, device=dev)
     ws_acc = torch.empty(max(sv.workspace_size(sv.OP_ACCEPT, B, T, V=V), 256), dtype=torch.uint8, device=dev)
-    tgt = d["target_logits"].view(B, T, V)
-    dr = None if d["draft_logits"] is None else d["draft_logits"].view(B, T, V)
     modes = accept_modes(w)
     acc = [dict(accept_len=torch.empty((B,), **i32), path=torch.empty((B, T), **i32),
                 out_tokens=torch.empty((B, T), **i32), bonus=torch.empty((B,), **i32),
                 status=torch.empty((B,), **i32)) for _ in modes]
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
-    def attn_call():
-        sv.tree_attn(d["q"], d["k"], d["v"], d["kv_len"], d["parent"], out, k_scale=d["k_scale"],
-                     v_scale=d["v_scale"], lse=lse, status=st_a, workspace=ws_attn)
+    def make_calls(dd):
+        """The step's calls on the inputs in `dd` (outputs and workspaces shared)."""
+        tg = dd["target_logits"].view(B, T, V)
+        dl = None if dd["draft_logits"] is None else dd["draft_logits"].view(B, T, V)
 
-    def accept_call(i):
-        label, temp, with_draft = modes[i]
-        a = acc[i]
+        def attn_call():
+            sv.tree_attn(dd["q"], dd["k"], dd["v"], dd["kv_len"], dd["parent"], out, k_scale=dd["k_scale"],
+                         v_scale=dd["v_scale"], lse=lse, status=st_a, workspace=ws_attn)
 
-        def call():
-            sv.accept(tgt, d["tokens"], d["parent"], a["accept_len"], a["path"], a["out_tokens"], a["bonus"],
-                      draft_logits=dr if with_draft else None, temperature=temp,
-                      uniforms=d["uniforms"] if temp > 0 else None, status=a["status"], workspace=ws_acc)
-        return call
+        def accept_call(i):
+            label, temp, with_draft = modes[i]
+            a = acc[i]
 
-    calls = [attn_call] + [accept_call(i) for i in range(len(modes))]
+            def call():
+                sv.accept(tg, dd["tokens"], dd["parent"], a["accept_len"], a["path"], a["out_tokens"], a["bonus"],
+                          draft_logits=dl if with_draft else None, temperature=temp,
+                          uniforms=dd["uniforms"] if temp > 0 else None, status=a["status"], workspace=ws_acc)
+            return call
+
+        return [attn_call] + [accept_call(i) for i in range(len(modes))]
+
+    calls = make_calls(d)
 
     def check(what):
         assert (st_a == 0).all(), f"{what}: attention reported a per-request error"
@@ -444,16 +459,18 @@ def run_sv_verify(args, w):
                 h = torch.empty(d[k].shape, dtype=d[k].dtype).pin_memory()
                 h.copy_(d[k])
                 host[k] = h
+        d2 = {k: (None if t is None else torch.empty_like(t)) for k, t in d.items()}
         outs = {"out": out, "lse": lse}
         for i, a in enumerate(acc):
             outs.update({f"{k}_{modes[i][0]}": t for k, t in a.items()})
         n_e2e = max(3, args.steps // 2)
-        ms_e2e, h2d, d2h = e2e_time(host, d, calls, outs, n_e2e, stream)
+        ms_e2e, h2d, d2h = e2e_time(host, [d, d2], [calls, make_calls(d2)], outs, n_e2e, stream)
         e2e = {"value": B * T / (ms_e2e * 1e-3), "unit": "nodes/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e2e, "steps": n_e2e,
-               "copies": "inputs from pinned host memory (the three largest on their own streams), outputs back"}
+               "copies": ("every input from pinned host memory each step, on a copy stream into one of two device "
+                          "input sets while the previous step computes; outputs back each step")}
         check("end-to-end steps")
-        del host
+        del host, d2
 
     pk, pk_kind = peaks()
     ab = attn_bytes(w)
@@ -533,7 +550,12 @@ def run_sv_loss(args, lb):
             h = torch.empty(t.shape, dtype=t.dtype).pin_memory()
             h.copy_(t)
             host[k] = h
-        ms_e2e, h2d, d2h = e2e_time(host, d, [call], {"row_loss": rl, "sums": sums, "grad": grad},
+        d2 = {k: torch.empty_like(t) for k, t in d.items()}
+
+        def call2():
+            sv.loss(d2["logits"], d2["tokens"], d2["parent"], d2["labels"], rl, sums, grad=grad, status=st,
+                    workspace=ws)
+        ms_e2e, h2d, d2h = e2e_time(host, [d, d2], [[call], [call2]], {"row_loss": rl, "sums": sums, "grad": grad},
                                     max(3, args.steps // 2), stream)
         e2e = {"value": N * T / (ms_e2e * 1e-3), "unit": "trace nodes/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e2e}
