@@ -324,6 +324,7 @@ size_t attn_bwd_workspace_size(int B, int T, int Hq) {
 
 cudaError_t launch_attn_bwd(const AttnBwdArgs& a, cudaStream_t s) {
     if (a.B == 0) return cudaSuccess;
+    if (attn_bwd_tc_supported(a)) return launch_attn_bwd_tc(a, s);   // bf16, D = 128: tensor cores
     if (a.q_dt == SV_F32) return a.kv_dt == SV_F32 ? launch_typed<SV_F32, SV_F32>(a, s) : launch_typed<SV_F32, SV_BF16>(a, s);
     return a.kv_dt == SV_F32 ? launch_typed<SV_BF16, SV_F32>(a, s) : launch_typed<SV_BF16, SV_BF16>(a, s);
 }

@@ -156,6 +156,8 @@ struct AttnBwdArgs {
 
 size_t attn_bwd_workspace_size(int B, int T, int Hq);
 cudaError_t launch_attn_bwd(const AttnBwdArgs& a, cudaStream_t s);
+bool attn_bwd_tc_supported(const AttnBwdArgs& a);
+cudaError_t launch_attn_bwd_tc(const AttnBwdArgs& a, cudaStream_t s);
 
 struct CompactArgs {
     int B, T, Hkv, D, kv_cap;
