@@ -734,7 +734,8 @@ def run_ops(args):
         tf = flops / (us * 1e-6) / 1e12
         print(json.dumps({"workload": name, "op": "tree_attn_bwd", "us": round(us, 1), "TFLOP_s": round(tf, 2),
                           "tensor_frac": round(tf / pk["bf16_tflops"], 4),
-                          "note": "FLOPs = 10*D per (query row, allowed position)"}), flush=True)
+                          "note": ("tensor cores" if (w.q_dt == "bf16" and w.kv_dt == "bf16" and w.D == 128) else "CUDA cores")
+                                  + "; FLOPs = 10*D per (query row, allowed position)"}), flush=True)
 
     def paged_case(name, w, page_size=128):
         """Tree attention over the same caches scattered into a page pool; bytes as for the contiguous call."""

@@ -81,3 +81,21 @@ def test_attn_bwd_llama3_shape_two_requests():
     bf16, prefixes of 2048..8192)."""
     w, dout = make(0, B=2, T=60, Hq=32, Hkv=8, D=128, L=(2048, 8192), dt="bf16", tree=(4, 3, 2, 2, 1, 1))
     assert (check(w, dout) == 0).all()
+
+
+@pytest.mark.parametrize("Hq,Hkv,tree,T", [(8, 8, (3, 2, 2), 13), (64, 8, (4, 3, 2, 2, 1, 1, 1), 64),
+                                          (16, 2, "chain", 6)])
+def test_attn_bwd_tensor_core_groups(Hq, Hkv, tree, T):
+    # the tensor-core kernels (bf16, D = 128) at group sizes 1, 8 and 8 with 512 query rows per kv head (four
+    # 128-row tiles), prefixes that end inside a tile, NaN junk past every tree block
+    w, dout = make(Hq * T, B=2, T=T, Hq=Hq, Hkv=Hkv, D=128, L=(1, 700), dt="bf16", tree=tree)
+    assert (check(w, dout) == 0).all()
+
+
+def test_attn_bwd_tensor_core_statuses():
+    w, dout = make(5, B=3, T=13, Hq=16, Hkv=4, D=128, L=(100, 400), dt="bf16", tree=(3, 2, 2))
+    w.parent = w.parent.copy()
+    w.kv_len = w.kv_len.copy()
+    w.parent[1, 3] = 7
+    w.kv_len[2] = -1
+    assert list(check(w, dout)) == [0, 2, 1]
