@@ -37,6 +37,7 @@ typedef unsigned __int128 u128;
 
 constexpr int kRowThreads = 256;
 constexpr int kWalkThreads = 512;
+constexpr int kLazySumsMinT = 16;   // nodes per request from which the walk computes the weight sums itself
 constexpr int kMaxCluster = 8;
 
 struct RowStat {
@@ -169,6 +170,7 @@ __global__ void __launch_bounds__(kRowThreads) accept_rows_kernel(AcceptArgs a, 
     cg::cluster_group cluster = cg::this_cluster();
     __shared__ RowPart s_warp[kRowThreads / 32];
     __shared__ RowPart s_part;   // this CTA's partial, read by the whole cluster
+    __shared__ float s_wymin[kRowThreads / 32], s_ymin;   // stochastic rows: min y per warp, per CTA
 
     const int rank = (int)cluster.block_rank();
     const int row = blockIdx.x / CL;
@@ -202,9 +204,11 @@ __global__ void __launch_bounds__(kRowThreads) accept_rows_kernel(AcceptArgs a, 
     } else {
         for (int k = c0 + tid; k < c1; k += kRowThreads) visit(LG::load(base + k), k);
     }
+    float ymin = INFINITY;
     if (STOCH) {
         ymax = __fmul_rn(zmax, invT);
-        yfin = (zmax == -INFINITY || isfinite(ymax)) && (zmin == INFINITY || isfinite(__fmul_rn(zmin, invT)));
+        ymin = zmin == INFINITY ? INFINITY : __fmul_rn(zmin, invT);
+        yfin = (zmax == -INFINITY || isfinite(ymax)) && (zmin == INFINITY || isfinite(ymin));
     }
     // block combine
 #pragma unroll
@@ -213,6 +217,11 @@ __global__ void __launch_bounds__(kRowThreads) accept_rows_kernel(AcceptArgs a, 
         int i2 = __shfl_xor_sync(0xffffffffu, zarg, o);
         argmax_combine(zmax, zarg, v2, i2);
         ymax = fmaxf(ymax, __shfl_xor_sync(0xffffffffu, ymax, o));
+    }
+    if (STOCH) {
+#pragma unroll
+        for (int o = 16; o; o >>= 1) ymin = fminf(ymin, __shfl_xor_sync(0xffffffffu, ymin, o));
+        if (lane == 0) s_wymin[warp] = ymin;
     }
     zfin = __all_sync(0xffffffffu, zfin);
     yfin = __all_sync(0xffffffffu, yfin);
@@ -226,6 +235,11 @@ __global__ void __launch_bounds__(kRowThreads) accept_rows_kernel(AcceptArgs a, 
             p.fin &= s_warp[w].fin;
         }
         s_part = p;
+        if (STOCH) {
+            float m = s_wymin[0];
+            for (int w = 1; w < kRowThreads / 32; ++w) m = fminf(m, s_wymin[w]);
+            s_ymin = m;
+        }
     }
     // z-finiteness of this CTA (for the argmax output)
     __shared__ int s_zfin;
@@ -234,18 +248,21 @@ __global__ void __launch_bounds__(kRowThreads) accept_rows_kernel(AcceptArgs a, 
     cluster.sync();
     // cluster combine: every CTA reads every partial, so all agree on the row maximum
     RowPart tot = *cluster.map_shared_rank(&s_part, 0);
+    float tot_ymin = STOCH ? *cluster.map_shared_rank(&s_ymin, 0) : INFINITY;
     int zfin_all = *cluster.map_shared_rank(&s_zfin, 0);
     for (int q = 1; q < CL; ++q) {
         RowPart p = *cluster.map_shared_rank(&s_part, q);
         argmax_combine(tot.zmax, tot.zarg, p.zmax, p.zarg);
         tot.ymax = fmaxf(tot.ymax, p.ymax);
         tot.fin &= p.fin;
+        if (STOCH) tot_ymin = fminf(tot_ymin, *cluster.map_shared_rank(&s_ymin, q));
         zfin_all &= *cluster.map_shared_rank(&s_zfin, q);
     }
     cluster.sync();   // partials consumed; s_part may be reused
 
     u64 S = 0;
-    if (STOCH && tot.fin) {
+    const bool sums = STOCH && !a.lazy_sums;   // else the walk computes the sums of the rows it visits
+    if (sums && tot.fin) {
         const float m = tot.ymax;
         if (vec_ok) {
 #pragma unroll 2
@@ -264,7 +281,7 @@ __global__ void __launch_bounds__(kRowThreads) accept_rows_kernel(AcceptArgs a, 
             for (int k = c0 + tid; k < c1; k += kRowThreads) S += fx_weight(__fmul_rn(LG::load(base + k), invT), m);
         }
     }
-    if (STOCH) {
+    if (sums) {
         S = warp_sum_u64(S);
         __shared__ u64 s_ws[kRowThreads / 32];
         if (lane == 0) s_ws[warp] = S;
@@ -287,8 +304,11 @@ __global__ void __launch_bounds__(kRowThreads) accept_rows_kernel(AcceptArgs a, 
         st.zmax = tot.zmax;
         st.arg = zfin_all ? tot.zarg : -1;
         st.ymax = tot.ymax;
-        st.fin = STOCH ? (tot.fin ? 2 : 0) : zfin_all;   // 2: finite, range of y not examined
-        st.S = STOCH ? tot.S : 0;
+        // stochastic: 1 finite with every t = (y - max y) log2 e above -2^22 (the shift form of the weights
+        // applies), 2 finite otherwise, 0 non-finite
+        const bool fast = tot.fin && __fsub_rn(tot.ymax, tot_ymin) < 2097152.0f;
+        st.fin = STOCH ? (tot.fin ? (fast ? 1 : 2) : 0) : zfin_all;
+        st.S = sums ? tot.S : 0;
         ((RowStat*)a.ws)[row] = st;
         if (a.argmax && !is_draft) a.argmax[r] = st.arg;
     }
@@ -562,11 +582,13 @@ struct WalkShared {
     ResidStep rs[SV_MAX_T];   // PROB: the integer constants of each rejection step
     u64 red[kWalkThreads / 32];
     u64 cta_sum;              // this CTA's share of a cluster-wide sum (read remotely)
+    u64 redq[kWalkThreads / 32];
+    u64 cta_sumq;             // the same for the draft row's weights
     int32_t found;            // sampled index found in this CTA (-1 if not)
     int st;
 };
 
-template <int LDT, int MODE>
+template <int LDT, int MODE, bool LAZY>
 __global__ void __launch_bounds__(kWalkThreads, 2) accept_walk_kernel(AcceptArgs a, int CLW) {
     using LG = Logit<LDT>;
     using LT = typename LG::T;
@@ -658,7 +680,7 @@ __global__ void __launch_bounds__(kWalkThreads, 2) accept_walk_kernel(AcceptArgs
             const LT* prow_p = P + prow * V;
             const LT* prow_q = (MODE == MODE_PROB) ? Q + prow * V : nullptr;
             int nrej = 0;
-            u64 Sres = sp.S;
+            u64 Sp = sp.S;   // the row's weight sum (computed below when the row kernel left it to the walk)
             // residual weight of token k (target logit zp, draft logit zq) after the rejections so far
             auto wres_z = [&](float zp, float zq, int k) -> u64 {
                 u64 w = fx_weight(__fmul_rn(zp, invT), sp.ymax);
@@ -736,9 +758,65 @@ __global__ void __launch_bounds__(kWalkThreads, 2) accept_walk_kernel(AcceptArgs
                     sh.cta_sum = t;
                 }
             };
+            // the weight sums of this row (and of the draft's row) over the cluster, when the row kernel left them to
+            // the walk, in one pass over both rows: the plain sums of row p then stay in sh.red / sh.cta_sum for a
+            // bonus draw from the row itself
+            bool plain_valid = false;
+            if (LAZY) {
+                u64 ws = 0, wsq = 0;
+                if (vec_ok) {
+                    for (int k = s0 + lane * VEC; k < s1; k += 32 * VEC) {
+                        float z[VEC], zq[VEC];
+                        LG::load_vec(prow_p + k, z);
+                        if (MODE == MODE_PROB) LG::load_vec(prow_q + k, zq);
+#pragma unroll
+                        for (int e = 0; e < VEC; e += 2) {
+                            uint32_t w0, w1;
+                            if (fastp) fx_weight2_fast<false>(z[e], z[e + 1], invT, sp.ymax, w0, w1);
+                            else { w0 = fx_weight(__fmul_rn(z[e], invT), sp.ymax); w1 = fx_weight(__fmul_rn(z[e + 1], invT), sp.ymax); }
+                            ws += (u64)w0 + w1;
+                            if (MODE == MODE_PROB) {
+                                if (fastq) fx_weight2_fast<false>(zq[e], zq[e + 1], invT, sq.ymax, w0, w1);
+                                else { w0 = fx_weight(__fmul_rn(zq[e], invT), sq.ymax); w1 = fx_weight(__fmul_rn(zq[e + 1], invT), sq.ymax); }
+                                wsq += (u64)w0 + w1;
+                            }
+                        }
+                    }
+                } else {
+                    for (int k = s0 + lane; k < s1; k += 32) {
+                        ws += fx_weight(__fmul_rn(LG::load(prow_p + k), invT), sp.ymax);
+                        if (MODE == MODE_PROB) wsq += fx_weight(__fmul_rn(LG::load(prow_q + k), invT), sq.ymax);
+                    }
+                }
+                ws = warp_sum_u64(ws);
+                if (MODE == MODE_PROB) wsq = warp_sum_u64(wsq);
+                if (lane == 0) {
+                    sh.red[warp] = ws;
+                    if (MODE == MODE_PROB) sh.redq[warp] = wsq;
+                }
+                __syncthreads();
+                if (tid == 0) {
+                    u64 t = 0, tq = 0;
+                    for (int w = 0; w < nw; ++w) {
+                        t += sh.red[w];
+                        if (MODE == MODE_PROB) tq += sh.redq[w];
+                    }
+                    sh.cta_sum = t;
+                    sh.cta_sumq = tq;
+                }
+                cluster.sync();
+                Sp = 0;
+                if (MODE == MODE_PROB) Sq = 0;
+                for (int q = 0; q < CLW; ++q) {
+                    Sp += *cluster.map_shared_rank(&sh.cta_sum, q);
+                    if (MODE == MODE_PROB) Sq += *cluster.map_shared_rank(&sh.cta_sumq, q);
+                }
+                cluster.sync();
+                plain_valid = true;
+            }
+            u64 Sres = Sp;
             bool sums_valid = false;   // sh.red / sh.cta_sum hold the current residual
             int next = -1, has_child = 0;
-            sums_valid = false;
             for (int c = cur + 1; c < T; ++c) {
                 if (sh.par[c] != cur) continue;
                 has_child = 1;
@@ -762,6 +840,7 @@ __global__ void __launch_bounds__(kWalkThreads, 2) accept_walk_kernel(AcceptArgs
                     __syncthreads();
                     ++nrej;
                     Sres = 0;  // recomputed below, in the layout the bonus draw searches
+                    plain_valid = false;
                     seg_sums();
                     cluster.sync();
                     for (int q = 0; q < CLW; ++q) Sres += *cluster.map_shared_rank(&sh.cta_sum, q);
@@ -778,11 +857,11 @@ __global__ void __launch_bounds__(kWalkThreads, 2) accept_walk_kernel(AcceptArgs
             }
             // the walk stops at `cur`: draw the bonus token from the residual (or the row itself)
             const bool use_res = has_child && Sres != 0;
-            const u64 R = use_res ? Sres : sp.S;
+            const u64 R = use_res ? Sres : Sp;
             if (!use_res) nrej = 0;
             const u128 thr = ((u128)U[0] * R) >> 32;
-            // the last residual pass already left the sums of the residual the draw uses
-            if (!(use_res && sums_valid)) seg_sums();
+            // the last residual pass (or the row's own sums) already left the sums the draw searches
+            if (!(use_res && sums_valid) && !(!use_res && plain_valid)) seg_sums();
             if (tid == 0) sh.found = -1;
             cluster.sync();
             u64 before = 0;   // weight mass of the CTAs before this one
@@ -886,9 +965,16 @@ int pick_cluster(int V, int per_cta) {
 }
 
 template <int LDT>
-cudaError_t launch_typed(const AcceptArgs& a, cudaStream_t s) {
+cudaError_t launch_typed(const AcceptArgs& args, cudaStream_t s) {
     constexpr int VEC = Logit<LDT>::kVec;
-    const bool stoch = a.temperature > 0.f;
+    const bool stoch = args.temperature > 0.f;
+    // Stochastic rows of a tree with many more nodes than a walk visits (T >= 16): the row kernel takes only
+    // the max, min and first argmax of every row (every row must still be checked for non-finite logits), and
+    // the walk computes the weight sums of the rows it visits.  Chains and small trees, whose walks visit most
+    // rows, compute every row's sums in the row pass (measured on 32 chains of 6 nodes: 103 us eager against
+    // 128 us lazy; on 8 trees of 60 nodes 89 against 76 us, on 128 trees of 64 nodes 1040 against 498 us).
+    AcceptArgs a = args;
+    a.lazy_sums = (stoch && a.T >= kLazySumsMinT) ? 1 : 0;
     const int mode = !stoch ? MODE_GREEDY : (a.draft ? MODE_PROB : MODE_ONEHOT);
     const int rows_src = a.B * a.T;
     const int rows = rows_src * (mode == MODE_PROB ? 2 : 1);
@@ -896,7 +982,7 @@ cudaError_t launch_typed(const AcceptArgs& a, cudaStream_t s) {
     // splits each row.  Greedy rows: the largest power-of-two cluster with at most about 9 CTAs per SM in
     // all, which evens out the last wave (measured on 480 and 192 rows of 128K-152K logits: 2 and 4).
     int CL;
-    if (stoch) {
+    if (stoch && !a.lazy_sums) {
         CL = rows >= 8 * sm_count() ? 1 : pick_cluster(a.V, kRowThreads * VEC * 4);
     } else {
         const int cap = pick_cluster(a.V, kRowThreads * VEC * 4);
@@ -912,7 +998,7 @@ cudaError_t launch_typed(const AcceptArgs& a, cudaStream_t s) {
     const long long row_bytes = (long long)a.V * 2;
     while (CLs < kMaxCluster && row_bytes > (long long)CLs * 40 * 1024) CLs *= 2;
     int chunk_s = ((a.V + CLs - 1) / CLs + 7) / 8 * 8;
-    const bool staged = stoch && LDT == SV_BF16 && a.V % 8 == 0 && (long long)chunk_s * 2 <= kStoMaxSlice;
+    const bool staged = stoch && !a.lazy_sums && LDT == SV_BF16 && a.V % 8 == 0 && (long long)chunk_s * 2 <= kStoMaxSlice;
     if (staged) {
         const size_t smem = (size_t)chunk_s * 2;
         // room for the slice, and the whole unified L1 as shared memory so several CTAs fit on an SM; function
@@ -941,10 +1027,15 @@ cudaError_t launch_typed(const AcceptArgs& a, cudaStream_t s) {
         const int cap = pick_cluster(a.V, kWalkThreads * 8);
         while (CLW * 2 <= cap && (long long)a.B * CLW * 2 <= 2LL * sm_count()) CLW *= 2;
     }
+    const dim3 gw(a.B * CLW), bw(kWalkThreads);
     switch (mode) {
-    case MODE_GREEDY: return launch_ex(accept_walk_kernel<LDT, MODE_GREEDY>, dim3(a.B), dim3(kWalkThreads), 0, s, 1, true, a, 1);
-    case MODE_PROB:   return launch_ex(accept_walk_kernel<LDT, MODE_PROB>, dim3(a.B * CLW), dim3(kWalkThreads), 0, s, CLW, true, a, CLW);
-    default:          return launch_ex(accept_walk_kernel<LDT, MODE_ONEHOT>, dim3(a.B * CLW), dim3(kWalkThreads), 0, s, CLW, true, a, CLW);
+    case MODE_GREEDY: return launch_ex(accept_walk_kernel<LDT, MODE_GREEDY, false>, gw, bw, 0, s, 1, true, a, 1);
+    case MODE_PROB:
+        if (a.lazy_sums) return launch_ex(accept_walk_kernel<LDT, MODE_PROB, true>, gw, bw, 0, s, CLW, true, a, CLW);
+        return launch_ex(accept_walk_kernel<LDT, MODE_PROB, false>, gw, bw, 0, s, CLW, true, a, CLW);
+    default:
+        if (a.lazy_sums) return launch_ex(accept_walk_kernel<LDT, MODE_ONEHOT, true>, gw, bw, 0, s, CLW, true, a, CLW);
+        return launch_ex(accept_walk_kernel<LDT, MODE_ONEHOT, false>, gw, bw, 0, s, CLW, true, a, CLW);
     }
 }
 

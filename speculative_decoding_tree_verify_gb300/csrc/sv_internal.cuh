@@ -112,6 +112,9 @@ struct AcceptArgs {
     int32_t* argmax;
     int32_t* status;
     void* ws;
+    // stochastic modes: the row kernel leaves the weight sums to the walk, which computes them for the rows it
+    // visits only
+    int lazy_sums = 0;
 };
 
 size_t accept_workspace_size(int B, int T, int V);

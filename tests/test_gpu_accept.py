@@ -61,6 +61,84 @@ def test_stochastic_parity(mode, temp, V, dt, tree, T):
     assert (g["status"] == 0).all()
 
 
+# Trees of 16 nodes or more: the row kernel leaves the weight sums to the walk, which computes them for the
+# rows it visits only (the chains and small trees above take the sums in the row pass).
+LAZY_TREES = [((2, 2, 2, 2, 1), 25), ((4, 3, 2, 2, 1, 1, 1), 64), ("star", 16)]
+
+
+@pytest.mark.parametrize("mode", ["prob", "onehot"])
+@pytest.mark.parametrize("temp", [1.0, 1e-3])
+@pytest.mark.parametrize("V,dt", [(16, "f32"), (1000, "bf16"), (4099, "f32"), (50000, "bf16")])
+@pytest.mark.parametrize("tree,T", LAZY_TREES)
+def test_stochastic_parity_walk_sums(mode, temp, V, dt, tree, T):
+    if tree == "star" and T > V:
+        pytest.skip("star needs V >= T")
+    w = W.make_verify(V * 5 + T, B=19, T=T, Hq=1, Hkv=1, D=8, L=(0, 0), V=V, logit_dt=dt, tree=tree,
+                      mode=mode, temperature=temp, force_p=0.7, sigma=2.5, with_attn=False)
+    g = check(w, temperature=temp, draft=w.draft_logits if mode == "prob" else None)
+    assert (g["status"] == 0).all()
+
+
+@pytest.mark.parametrize("mode", ["prob", "onehot"])
+def test_stochastic_parity_walk_sums_full_vocabulary(mode):
+    V, T = 151936, 25
+    w = W.make_verify(V + 5, B=7, T=T, Hq=1, Hkv=1, D=8, L=(0, 0), V=V, logit_dt="bf16", tree=(2, 2, 2, 2, 1),
+                      mode=mode, temperature=0.6, force_p=0.7, sigma=2.5, with_attn=False)
+    g = check(w, temperature=0.6, draft=w.draft_logits if mode == "prob" else None)
+    assert (g["status"] == 0).all()
+
+
+@pytest.mark.parametrize("mode", ["prob", "onehot"])
+def test_walk_sums_wide_range_and_statuses(mode):
+    """Trees of 25 nodes: rows holding a logit about 4e6 below the rest take the scalar weights in the walk's
+    own sum pass; non-finite logits and y overflow fail their request whether or not the walk visits the row."""
+    w = W.make_verify(31, B=8, T=25, Hq=1, Hkv=1, D=8, L=(0, 0), V=3000, logit_dt="bf16", tree=(2, 2, 2, 2, 1),
+                      mode=mode, temperature=0.9, force_p=0.8, sigma=2.0, with_attn=False)
+    w.target_logits = w.target_logits.copy()
+    low = W.f32_to_bf16(np.float32(-4.0e6))
+    w.target_logits[::2, :, 17] = low
+    if mode == "prob":
+        w.draft_logits = w.draft_logits.copy()
+        w.draft_logits[1::3, :, 2999] = low
+    for want in (False, True):
+        g = check_opts(w, 0.9, w.draft_logits if mode == "prob" else None, want)
+        assert (g["status"] == 0).all()
+    w.target_logits[1, 24, 100] = 0x7FC0                                  # NaN in a leaf row
+    w.target_logits[2, 0, 5] = 0xFF80                                     # -inf in the root row
+    w.target_logits[3, 13, 2047] = W.f32_to_bf16(np.float32(3.0e37))[0]   # y = 3.3e37 / 0.9 stays finite
+    w.target_logits[4, 7, 1] = W.f32_to_bf16(np.float32(3.3e38))[0]       # y overflows float32
+    g = check_opts(w, 0.9, w.draft_logits if mode == "prob" else None, True)
+    assert list(g["status"]) == [0, 5, 5, 0, 5, 0, 0, 0]
+
+
+@pytest.mark.parametrize("V,dt,temp", [(151936, "bf16", 1.0), (50000, "bf16", 0.8), (4096, "f32", 0.7),
+                                       (40003, "bf16", 1.0), (128256, "bf16", 0.3)])
+def test_bonus_draw_at_prefix_boundaries_walk_sums(V, dt, temp):
+    """Trees of 17 nodes (ONEHOT, the walk computes the sums): the root's only child carries a token whose
+    target weight is 0, so it is always rejected and the bonus is drawn from a residual equal to the root's row;
+    the slot-0 uniform on a prefix-sum boundary of that row pins the walk's sums and prefix sums to the unit."""
+    T = 17
+    w = W.make_verify(V + 91, B=48, T=T, Hq=1, Hkv=1, D=8, L=(0, 0), V=V, logit_dt=dt, tree="chain",
+                      mode="onehot", temperature=temp, force_p=0.0, sigma=2.5, with_attn=False)   # no forced peaks
+    w.target_logits = w.target_logits.copy()
+    w.parent = np.full((w.B, T), 1, np.int32)
+    w.parent[:, 0] = -1
+    w.parent[:, 1] = 0
+    w.tokens = w.tokens.copy()
+    low = np.ravel(W.f32_to_bf16(np.float32(-4.0e6)))[0] if dt == "bf16" else np.float32(-4.0e6)
+    for b in range(w.B):
+        x = (7 * b + 5) % V
+        w.tokens[b, 1] = x
+        w.target_logits[b, 0, x] = low                 # weight 0: the child is rejected whatever its uniform
+    w.target_logits[1::4, 0, 3] = low                  # a quarter of the rows span more than 2^21 in y
+    u = w.uniforms.copy()
+    u[:, 0] = boundary_uniforms(w, temp, V)[:, 0]
+    w.uniforms = u
+    for want in (False, True):
+        g = check_opts(w, temp, None, want)
+        assert (g["status"] == 0).all() and (g["accept_len"] == 0).all()
+
+
 def test_single_node_trees():
     for t in (0.0, 1.0):
         w = W.make_verify(3, B=9, T=1, Hq=1, Hkv=1, D=8, L=(0, 0), V=777, logit_dt="bf16", tree="chain",
@@ -174,6 +252,8 @@ def boundary_uniforms(w, temperature, seed, wide_rows=()):
         S = int(wts.sum())
         cs = np.cumsum(wts)
         cand = np.nonzero((wts > 0) & (cs * 2 >= S) & (cs < S))[0]
+        if cand.size == 0:   # the last token of weight > 0 holds the upper half: any inner boundary
+            cand = np.nonzero((wts > 0) & (cs < S))[0]
         j = int(rng.choice(cand))
         up = -(-(int(cs[j]) << 32) // S)               # ceil(cs[j] * 2^32 / S)
         u[b, 0] = up - 1 if b % 2 == 0 else up
