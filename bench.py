@@ -331,13 +331,35 @@ def timed_graph_steps(graphs, steps, flush, stream, clock_index):
     return per_call, clk.summary()
 
 
-def e2e_time(host, dev_sets, call_sets, outs_dev, steps, stream):
+def prefix_rows(kv_len, T, Hkv, kv_cap):
+    """The slices of a [B, Hkv, kv_cap, D] cache that a step reads: for every request b and kv head h the first
+    kv_len[b] + T positions (the prefix and the tree's own K/V), each one contiguous run of memory."""
+    out = []
+    for b, L in enumerate(kv_len):
+        n = min(int(L) + int(T), int(kv_cap))
+        out.extend((b, h, n) for h in range(Hkv))
+    return out
+
+
+def e2e_time(host, dev_sets, call_sets, outs_dev, steps, stream, prefix=None):
     """Per-step time (ms) through the API with every input copied from pinned host memory and the outputs
     copied back, each step.  Two device copies of the inputs (`dev_sets`, with `call_sets` the calls bound to
     each) let the next step's host-to-device copies, on their own stream, run while the current step computes;
     a step's compute waits for its own copies, and a copy into a set waits until the step that last read it is
-    done.  The timed region spans the first step's copies to the last step's outputs."""
+    done.  The timed region spans the first step's copies to the last step's outputs.  `prefix` maps a cache
+    key to `prefix_rows(...)`: only those runs of the cache are copied (the rest is never read)."""
     import torch
+    prefix = prefix or {}
+    # (destination, source) pairs of each device set, views made once outside the timed region
+    plans = []
+    for ds in dev_sets:
+        plan = []
+        for k, t in host.items():
+            if k in prefix:
+                plan.extend((ds[k][r, h, :n], t[r, h, :n]) for (r, h, n) in prefix[k])
+            else:
+                plan.append((ds[k], t))
+        plans.append(plan)
     outs_host = {k: torch.empty(t.shape, dtype=t.dtype).pin_memory() for k, t in outs_dev.items()}
     copy_stream = torch.cuda.Stream()
     copied = [torch.cuda.Event(), torch.cuda.Event()]
@@ -348,8 +370,8 @@ def e2e_time(host, dev_sets, call_sets, outs_dev, steps, stream):
     def h2d(b):
         copy_stream.wait_event(done[b])
         with torch.cuda.stream(copy_stream):
-            for k, t in host.items():
-                dev_sets[b][k].copy_(t, non_blocking=True)
+            for dst, src in plans[b]:
+                dst.copy_(src, non_blocking=True)
             copied[b].record(copy_stream)
 
     def run(n):
@@ -373,7 +395,13 @@ def e2e_time(host, dev_sets, call_sets, outs_dev, steps, stream):
     run(steps)
     t1.record(stream)
     torch.cuda.synchronize()
-    h2d_bytes = sum(t.numel() * t.element_size() for t in host.values())
+    h2d_bytes = 0
+    for k, t in host.items():
+        if k in prefix:
+            row = t[0, 0, 0].numel() * t.element_size()
+            h2d_bytes += sum(n for (_, _, n) in prefix[k]) * row
+        else:
+            h2d_bytes += t.numel() * t.element_size()
     d2h_bytes = sum(t.numel() * t.element_size() for t in outs_host.values())
     return t0.elapsed_time(t1) / steps, h2d_bytes, d2h_bytes
 
@@ -464,11 +492,14 @@ def run_sv_verify(args, w):
         for i, a in enumerate(acc):
             outs.update({f"{k}_{modes[i][0]}": t for k, t in a.items()})
         n_e2e = max(3, args.steps // 2)
-        ms_e2e, h2d, d2h = e2e_time(host, [d, d2], [calls, make_calls(d2)], outs, n_e2e, stream)
+        runs = prefix_rows(w.kv_len, T, w.Hkv, w.kv_cap)
+        ms_e2e, h2d, d2h = e2e_time(host, [d, d2], [calls, make_calls(d2)], outs, n_e2e, stream,
+                                    prefix={"k": runs, "v": runs})
         e2e = {"value": B * T / (ms_e2e * 1e-3), "unit": "nodes/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e2e, "steps": n_e2e,
-               "copies": ("every input from pinned host memory each step, on a copy stream into one of two device "
-                          "input sets while the previous step computes; outputs back each step")}
+               "copies": ("every input from pinned host memory each step (of the K/V caches, each request's "
+                          "kv_len + T positions per kv head, the part a step reads), on a copy stream into one of "
+                          "two device input sets while the previous step computes; outputs back each step")}
         check("end-to-end steps")
         del host, d2
 

@@ -37,7 +37,8 @@ typedef unsigned __int128 u128;
 
 constexpr int kRowThreads = 256;
 constexpr int kWalkThreads = 512;
-constexpr int kLazySumsMinT = 16;   // nodes per request from which the walk computes the weight sums itself
+constexpr int kLazySumsMinT = 16;
+constexpr int kSearchSteps = 8;     // warp steps of a bonus search above which the segment is split first   // nodes per request from which the walk computes the weight sums itself
 constexpr int kMaxCluster = 8;
 
 struct RowStat {
@@ -583,6 +584,7 @@ struct WalkShared {
     u64 red[kWalkThreads / 32];
     u64 cta_sum;              // this CTA's share of a cluster-wide sum (read remotely)
     u64 redq[kWalkThreads / 32];
+    u64 sub[kWalkThreads / 32];   // bonus search: the sums of the selected warp segment's sub-segments
     u64 cta_sumq;             // the same for the draft row's weights
     int32_t found;            // sampled index found in this CTA (-1 if not)
     int st;
@@ -861,7 +863,23 @@ __global__ void __launch_bounds__(kWalkThreads, 2) accept_walk_kernel(AcceptArgs
             if (!use_res) nrej = 0;
             const u128 thr = ((u128)U[0] * R) >> 32;
             // the last residual pass (or the row's own sums) already left the sums the draw searches
-            if (!(use_res && sums_valid) && !(!use_res && plain_valid)) seg_sums();
+            if (MODE == MODE_ONEHOT && use_res && plain_valid) {
+                // one-hot residual = the row's weights with the rejected tokens set to 0: take each distinct
+                // rejected token's weight off the sums of the warp segment and CTA that hold it
+                if (tid == 0) {
+                    for (int i = 0; i < nrej; ++i) {
+                        const int x = (int)sh.hist[i];
+                        bool dup = false;
+                        for (int j = 0; j < i; ++j) dup |= (int)sh.hist[j] == x;
+                        if (dup || x < k0 || x >= k1) continue;
+                        const u64 wx = fx_weight(__fmul_rn(LG::load(prow_p + x), invT), sp.ymax);
+                        sh.red[(x - k0) / seg] -= wx;
+                        sh.cta_sum -= wx;
+                    }
+                }
+            } else if (!(use_res && sums_valid) && !(!use_res && plain_valid)) {
+                seg_sums();
+            }
             if (tid == 0) sh.found = -1;
             cluster.sync();
             u64 before = 0;   // weight mass of the CTAs before this one
@@ -874,14 +892,40 @@ __global__ void __launch_bounds__(kWalkThreads, 2) accept_walk_kernel(AcceptArgs
                     if (thr < wb + sh.red[w]) { wsel = w; break; }
                     wb += sh.red[w];
                 }
-                if (warp == wsel && vec_ok) {
-                    // 32 * VEC tokens per step: each lane one vector, a warp scan of the lane totals
-                    u64 run = wb;
-                    for (int kb = s0; kb < s1; kb += 32 * VEC) {
+                if (vec_ok && wsel >= 0) {
+                    // A segment longer than kSearchSteps warp steps is split into nw sub-segments of whole
+                    // vectors, whose sums every warp computes at once; the warp of the segment (or sub-segment)
+                    // holding the draw then scans it, 32 * VEC tokens per step: each lane one vector, a warp scan
+                    // of the lane totals
+                    const int t0 = min(k1, k0 + wsel * seg), t1 = min(k1, t0 + seg);
+                    int u0 = t0, u1 = t1, usel = wsel;
+                    u64 ub = wb;
+                    if (t1 - t0 > kSearchSteps * 32 * VEC) {
+                        const int sub = ((t1 - t0 + nw - 1) / nw + VEC - 1) / VEC * VEC;
+                        u0 = min(t1, t0 + warp * sub);
+                        u1 = min(t1, u0 + sub);
+                        u64 us = 0;
+                        for (int k = u0 + lane * VEC; k < u1; k += 32 * VEC) {
+                            u64 w[VEC];
+                            wres_vec(k, w);
+#pragma unroll
+                            for (int e = 0; e < VEC; ++e) us += w[e];
+                        }
+                        us = warp_sum_u64(us);
+                        if (lane == 0) sh.sub[warp] = us;
+                        __syncthreads();
+                        usel = -1;
+                        for (int w = 0; w < nw; ++w) {
+                            if (thr < ub + sh.sub[w]) { usel = w; break; }
+                            ub += sh.sub[w];
+                        }
+                    }
+                    u64 run = ub;
+                    for (int kb = u0; warp == usel && kb < u1; kb += 32 * VEC) {
                         const int k = kb + lane * VEC;
                         u64 w[VEC];
                         u64 tl = 0;
-                        if (k < s1) {
+                        if (k < u1) {
                             wres_vec(k, w);
 #pragma unroll
                             for (int e = 0; e < VEC; ++e) tl += w[e];
@@ -892,7 +936,7 @@ __global__ void __launch_bounds__(kWalkThreads, 2) accept_walk_kernel(AcceptArgs
                             const u64 v = __shfl_up_sync(0xffffffffu, incl, o);
                             if (lane >= o) incl += v;
                         }
-                        const unsigned hit = __ballot_sync(0xffffffffu, k < s1 && (u128)run + incl > thr);
+                        const unsigned hit = __ballot_sync(0xffffffffu, k < u1 && (u128)run + incl > thr);
                         if (hit) {
                             if (lane == __ffs(hit) - 1) {
                                 u128 acc = (u128)run + (incl - tl);
@@ -907,7 +951,7 @@ __global__ void __launch_bounds__(kWalkThreads, 2) accept_walk_kernel(AcceptArgs
                         }
                         run += __shfl_sync(0xffffffffu, incl, 31);
                     }
-                } else if (warp == wsel) {
+                } else if (!vec_ok && warp == wsel) {
                     u64 run = wb;
                     for (int k = s0; k < s1; k += 32) {
                         u64 w = (k + lane < s1) ? wres(k + lane) : 0;

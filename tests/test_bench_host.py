@@ -68,6 +68,25 @@ def test_attention_work_counts_match_a_brute_force_count():
     assert bench.attn_bytes(w) == kv + 2 * w.B * w.T * w.Hq * w.D * 2 + w.B * w.T * w.Hq * 4 + w.B * (w.T + 1) * 4
 
 
+def test_end_to_end_cache_copies_cover_exactly_what_attention_reads():
+    """The end-to-end leg copies, per request and kv head, the first kv_len + T cache positions: one contiguous
+    run each in the [B, Hkv, kv_cap, D] layout, together the cache bytes of the attention's algorithmic count."""
+    w = W.make_verify(5, B=4, T=7, Hq=4, Hkv=2, D=16, L=(3, 30), V=16, q_dt="bf16", kv_dt="bf16", tree="chain")
+    runs = bench.prefix_rows(w.kv_len, w.T, w.Hkv, w.kv_cap)
+    assert sorted((b, h) for b, h, _ in runs) == [(b, h) for b in range(w.B) for h in range(w.Hkv)]
+    for b, h, n in runs:
+        assert n == int(w.kv_len[b]) + w.T <= w.kv_cap
+    cache_bytes = 2 * sum(n for _, _, n in runs) * w.D * 2
+    assert cache_bytes == sum(int(w.kv_len[b]) + w.T for b in range(w.B)) * w.Hkv * w.D * 2 * 2
+    src = np.arange(w.k.size, dtype=np.int64).reshape(w.k.shape)
+    dst = np.full_like(src, -1)
+    for b, h, n in runs:
+        dst[b, h, :n] = src[b, h, :n]
+    for b in range(w.B):
+        n = int(w.kv_len[b]) + w.T
+        assert (dst[b, :, :n] == src[b, :, :n]).all() and (dst[b, :, n:] == -1).all()
+
+
 def test_default_workload_runs_both_acceptance_modes():
     assert bench.parse([]).workload == "fp8_long_context"
     assert [m[0] for m in bench.workload_modes("fp8_long_context")] == ["greedy", "onehot"]

@@ -139,6 +139,43 @@ def test_bonus_draw_at_prefix_boundaries_walk_sums(V, dt, temp):
         assert (g["status"] == 0).all() and (g["accept_len"] == 0).all()
 
 
+@pytest.mark.parametrize("V,dt,temp", [(151936, "bf16", 1.0), (4096, "f32", 0.7), (40003, "bf16", 0.5)])
+def test_bonus_draw_after_duplicate_rejections_walk_sums(V, dt, temp):
+    """Trees of 17 nodes (ONEHOT, the walk computes the sums): the root's two children carry the same token x
+    (the root row's second-largest logit) with uniforms that reject any token short of all the mass, so x is
+    rejected twice and taken out of the residual once; the slot-0 uniform on a prefix-sum boundary of that
+    residual (the row with x's weight set to 0) pins the residual's sums to the unit."""
+    T = 17
+    w = W.make_verify(V + 13, B=40, T=T, Hq=1, Hkv=1, D=8, L=(0, 0), V=V, logit_dt=dt, tree="chain",
+                      mode="onehot", temperature=temp, force_p=0.0, sigma=2.5, with_attn=False)
+    w.target_logits = w.target_logits.copy()
+    w.parent = np.full((w.B, T), 1, np.int32)
+    w.parent[:, 0] = -1
+    w.parent[:, 2] = 0
+    w.parent[:, 1] = 0
+    w.tokens = w.tokens.copy()
+    xs = []
+    for b in range(w.B):
+        z = W.decode_f32(w.target_logits[b, 0], w.logit_dt)
+        x = int(np.argsort(z, kind="stable")[-2])
+        xs.append(x)
+        w.tokens[b, 1] = w.tokens[b, 2] = x
+    u = w.uniforms.copy()
+    u[:, 1] = u[:, 2] = 0xFFFFFFFF
+    resid = W.make_verify(V + 13, B=w.B, T=1, Hq=1, Hkv=1, D=8, L=(0, 0), V=V, logit_dt=dt, tree="chain",
+                          mode="onehot", temperature=temp, with_attn=False)
+    resid.target_logits = w.target_logits[:, :1].copy()
+    low = np.ravel(W.f32_to_bf16(np.float32(-4.0e6)))[0] if dt == "bf16" else np.float32(-4.0e6)
+    for b, x in enumerate(xs):
+        resid.target_logits[b, 0, x] = low               # the residual: x's weight 0, the row maximum unchanged
+    u[:, 0] = boundary_uniforms(resid, temp, V + 1)[:, 0]
+    w.uniforms = u
+    for want in (False, True):
+        g = check_opts(w, temp, None, want)
+        assert (g["status"] == 0).all() and (g["accept_len"] == 0).all()
+        assert all(int(g["bonus"][b]) != x for b, x in enumerate(xs))
+
+
 def test_single_node_trees():
     for t in (0.0, 1.0):
         w = W.make_verify(3, B=9, T=1, Hq=1, Hkv=1, D=8, L=(0, 0), V=777, logit_dt="bf16", tree="chain",
