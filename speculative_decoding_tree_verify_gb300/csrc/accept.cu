@@ -101,18 +101,10 @@ struct ResidStep {
     u64 a, b, F;
 };
 
-// floor(2^64 * b / d) for b < d < 2^63, by restoring division (once per rejection)
+// floor(2^64 * b / d) for b < d < 2^63 (the quotient fits 64 bits), by one 128-bit integer division (once
+// per rejection)
 __device__ u64 frac64(u64 b, u64 d) {
-    u64 q = 0, r = b;
-    for (int i = 0; i < 64; ++i) {
-        r <<= 1;
-        q <<= 1;
-        if (r >= d) {
-            r -= d;
-            q |= 1u;
-        }
-    }
-    return q;
+    return (u64)(((u128)b << 64) / (u128)d);
 }
 
 __device__ __forceinline__ u64 resid_step(u64 w, u64 wq64, const ResidStep& k, u64 d) {
@@ -631,7 +623,6 @@ __global__ void __launch_bounds__(kWalkThreads, 2) accept_walk_kernel(AcceptArgs
         if (__syncthreads_or(to)) st = SV_ERR_TIMEOUT;
         else if (__syncthreads_or(nf)) st = SV_ERR_NONFINITE;
     }
-    const bool writer = rank == 0 && tid == 0;
     if (st != SV_OK) {
         if (rank == 0) {
             for (int j = tid; j < T; j += kWalkThreads) {
@@ -649,18 +640,26 @@ __global__ void __launch_bounds__(kWalkThreads, 2) accept_walk_kernel(AcceptArgs
 
     int n = 0, cur = 0, bonus = -1;
     if (MODE == MODE_GREEDY) {
-        if (writer) {
+        // warp 0 walks: at each node the lanes test 32 later nodes at once (child of cur with the argmax token),
+        // and the lowest hit is the first such child
+        if (warp == 0) {
             for (;;) {
                 const int am = sh.arg[cur];
                 int next = -1;
-                for (int c = cur + 1; c < T; ++c)
-                    if (sh.par[c] == cur && sh.tok[c] == am) { next = c; break; }
+                for (int c0 = cur + 1; c0 < T; c0 += 32) {
+                    const int c = c0 + lane;
+                    const unsigned hit = __ballot_sync(0xffffffffu, c < T && sh.par[c] == cur && sh.tok[c] == am);
+                    if (hit) { next = c0 + __ffs(hit) - 1; break; }
+                }
                 if (next < 0) { bonus = am; break; }
-                sh.path[n++] = next;
+                if (lane == 0) sh.path[n] = next;
+                ++n;
                 cur = next;
             }
-            sh.st = n;
-            sh.found = bonus;
+            if (lane == 0) {
+                sh.st = n;
+                sh.found = bonus;
+            }
         }
         __syncthreads();
         n = sh.st;
