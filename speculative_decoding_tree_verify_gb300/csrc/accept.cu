@@ -37,8 +37,8 @@ typedef unsigned __int128 u128;
 
 constexpr int kRowThreads = 256;
 constexpr int kWalkThreads = 512;
-constexpr int kLazySumsMinT = 16;
-constexpr int kSearchSteps = 8;     // warp steps of a bonus search above which the segment is split first   // nodes per request from which the walk computes the weight sums itself
+constexpr int kLazySumsMinT = 16;   // nodes per request from which the walk computes the weight sums itself
+constexpr int kSearchSteps = 8;     // warp steps of a bonus search above which the segment is split first
 constexpr int kMaxCluster = 8;
 
 struct RowStat {
