@@ -699,7 +699,7 @@ __global__ void __launch_bounds__(kWalkThreads, 2) accept_walk_kernel(AcceptArgs
                 return wres_z(LG::load(prow_p + k), MODE == MODE_PROB ? LG::load(prow_q + k) : 0.f, k);
             };
             // the VEC residual weights of tokens k .. k+VEC-1 (16-byte loads; rows are 16-byte aligned)
-            // rows marked by the staged row kernel as having every t above -2^22 take the shift form of the
+            // rows marked by the row kernels as having every t above -2^22 take the shift form of the
             // weights (identical integers, fewer instructions)
             const bool fastp = sp.fin == 1;
             const bool fastq = MODE == MODE_PROB ? sq.fin == 1 : true;
@@ -1014,16 +1014,18 @@ cudaError_t launch_typed(const AcceptArgs& args, cudaStream_t s) {
     // Stochastic rows of a tree with many more nodes than a walk visits (T >= 16): the row kernel takes only
     // the max, min and first argmax of every row (every row must still be checked for non-finite logits), and
     // the walk computes the weight sums of the rows it visits.  Chains and small trees, whose walks visit most
-    // rows, compute every row's sums in the row pass (measured on 32 chains of 6 nodes: 103 us eager against
-    // 128 us lazy; on 8 trees of 60 nodes 89 against 76 us, on 128 trees of 64 nodes 1040 against 498 us).
+    // rows, compute every row's sums in the row pass (measured on 32 chains of 6 nodes: 103 us with the sums in
+    // the row pass against 110 us; on 8 trees of 60 nodes 89 against 76 us, on 128 trees of 64 nodes 1040
+    // against 498 us).
     AcceptArgs a = args;
     a.lazy_sums = (stoch && a.T >= kLazySumsMinT) ? 1 : 0;
     const int mode = !stoch ? MODE_GREEDY : (a.draft ? MODE_PROB : MODE_ONEHOT);
     const int rows_src = a.B * a.T;
     const int rows = rows_src * (mode == MODE_PROB ? 2 : 1);
-    // Stochastic rows: one CTA per row when there are many (no cluster synchronisation), else a cluster
-    // splits each row.  Greedy rows: the largest power-of-two cluster with at most about 9 CTAs per SM in
-    // all, which evens out the last wave (measured on 480 and 192 rows of 128K-152K logits: 2 and 4).
+    // Stochastic rows with their sums: one CTA per row when there are many (no cluster synchronisation), else a
+    // cluster splits each row.  Greedy rows and stochastic rows without sums: the largest power-of-two cluster
+    // with at most about 9 CTAs per SM in all, which evens out the last wave (measured on 480 and 192 rows of
+    // 128K-152K logits: 2 and 4).
     int CL;
     if (stoch && !a.lazy_sums) {
         CL = rows >= 8 * sm_count() ? 1 : pick_cluster(a.V, kRowThreads * VEC * 4);
