@@ -39,6 +39,7 @@ constexpr int kRowThreads = 256;
 constexpr int kWalkThreads = 512;
 constexpr int kLazySumsMinT = 16;   // nodes per request from which the walk computes the weight sums itself
 constexpr int kSearchSteps = 8;     // warp steps of a bonus search above which the segment is split first
+constexpr int kLazyLoads = 4;       // 16-byte loads in flight per lane in the walk's one-hot row-sum pass
 constexpr int kMaxCluster = 8;
 
 struct RowStat {
@@ -120,25 +121,27 @@ __device__ __forceinline__ u64 resid_step(u64 w, u64 wq64, const ResidStep& k, u
 template <int LDT> struct Logit;
 template <> struct Logit<SV_F32> {
     using T = float;
+    using Raw = float4;   // one 16-byte vector as loaded
     static constexpr int kVec = 4;
-    __device__ static void load_vec(const T* p, float* z) {
-        float4 v = __ldg(reinterpret_cast<const float4*>(p));
-        z[0] = v.x; z[1] = v.y; z[2] = v.z; z[3] = v.w;
-    }
+    __device__ static Raw load_raw(const T* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+    __device__ static void unpack(const Raw& v, float* z) { z[0] = v.x; z[1] = v.y; z[2] = v.z; z[3] = v.w; }
+    __device__ static void load_vec(const T* p, float* z) { unpack(load_raw(p), z); }
     __device__ static float load(const T* p) { return __ldg(p); }
 };
 template <> struct Logit<SV_BF16> {
     using T = uint16_t;
+    using Raw = uint4;
     static constexpr int kVec = 8;
-    __device__ static void load_vec(const T* p, float* z) {
-        uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
-        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    __device__ static Raw load_raw(const T* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+    __device__ static void unpack(const Raw& v, float* z) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             z[2 * i] = __uint_as_float(w[i] << 16);
             z[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
         }
     }
+    __device__ static void load_vec(const T* p, float* z) { unpack(load_raw(p), z); }
     __device__ static float load(const T* p) { return bf16_bits_to_float(__ldg(p)); }
 };
 
@@ -765,7 +768,29 @@ __global__ void __launch_bounds__(kWalkThreads, 2) accept_walk_kernel(AcceptArgs
             bool plain_valid = false;
             if (LAZY) {
                 u64 ws = 0, wsq = 0;
-                if (vec_ok) {
+                if (vec_ok && MODE == MODE_ONEHOT) {
+                    // one row: each lane keeps kLazyLoads 16-byte loads in flight
+                    for (int kb = s0 + lane * VEC; kb < s1; kb += kLazyLoads * 32 * VEC) {
+                        typename LG::Raw r[kLazyLoads];
+#pragma unroll
+                        for (int j = 0; j < kLazyLoads; ++j)
+                            if (kb + j * 32 * VEC < s1) r[j] = LG::load_raw(prow_p + kb + j * 32 * VEC);
+#pragma unroll
+                        for (int j = 0; j < kLazyLoads; ++j) {
+                            if (kb + j * 32 * VEC < s1) {
+                                float z[VEC];
+                                LG::unpack(r[j], z);
+#pragma unroll
+                                for (int e = 0; e < VEC; e += 2) {
+                                    uint32_t w0, w1;
+                                    if (fastp) fx_weight2_fast<false>(z[e], z[e + 1], invT, sp.ymax, w0, w1);
+                                    else { w0 = fx_weight(__fmul_rn(z[e], invT), sp.ymax); w1 = fx_weight(__fmul_rn(z[e + 1], invT), sp.ymax); }
+                                    ws += (u64)w0 + w1;
+                                }
+                            }
+                        }
+                    }
+                } else if (vec_ok) {
                     for (int k = s0 + lane * VEC; k < s1; k += 32 * VEC) {
                         float z[VEC], zq[VEC];
                         LG::load_vec(prow_p + k, z);
