@@ -580,6 +580,8 @@ struct WalkShared {
     u64 cta_sum;              // this CTA's share of a cluster-wide sum (read remotely)
     u64 redq[kWalkThreads / 32];
     u64 sub[kWalkThreads / 32];   // bonus search: the sums of the selected warp segment's sub-segments
+    float zc_p[SV_MAX_T], zc_q[SV_MAX_T];   // the current row's target (draft) logit at each child's token
+    uint32_t uc[SV_MAX_T];                  // and each child's uniform
     u64 cta_sumq;             // the same for the draft row's weights
     int32_t found;            // sampled index found in this CTA (-1 if not)
     int st;
@@ -765,6 +767,16 @@ __global__ void __launch_bounds__(kWalkThreads, 2) accept_walk_kernel(AcceptArgs
             // the weight sums of this row (and of the draft's row) over the cluster, when the row kernel left them to
             // the walk, in one pass over both rows: the plain sums of row p then stay in sh.red / sh.cta_sum for a
             // bonus draw from the row itself
+            // the logits and uniforms the acceptance tests of cur's children read, loaded at once
+            for (int c = cur + 1 + tid; c < T; c += kWalkThreads) {
+                if (sh.par[c] == cur) {
+                    const int x = sh.tok[c];
+                    sh.zc_p[c] = LG::load(prow_p + x);
+                    if (MODE == MODE_PROB) sh.zc_q[c] = LG::load(prow_q + x);
+                    sh.uc[c] = U[c];
+                }
+            }
+            if (!LAZY) __syncthreads();   // (the sum pass below synchronises the CTA otherwise)
             bool plain_valid = false;
             if (LAZY) {
                 u64 ws = 0, wsq = 0;
@@ -847,9 +859,9 @@ __global__ void __launch_bounds__(kWalkThreads, 2) accept_walk_kernel(AcceptArgs
                 if (sh.par[c] != cur) continue;
                 has_child = 1;
                 const int x = sh.tok[c];
-                const u64 wpx = wres(x);
-                const u64 wqx = (MODE == MODE_PROB) ? fx_weight(__fmul_rn(LG::load(prow_q + x), invT), sq.ymax) : 1u;
-                if ((u128)U[c] * wqx * Sres < (((u128)wpx * Sq) << 32)) { next = c; break; }
+                const u64 wpx = wres_z(sh.zc_p[c], MODE == MODE_PROB ? sh.zc_q[c] : 0.f, x);
+                const u64 wqx = (MODE == MODE_PROB) ? fx_weight(__fmul_rn(sh.zc_q[c], invT), sq.ymax) : 1u;
+                if ((u128)sh.uc[c] * wqx * Sres < (((u128)wpx * Sq) << 32)) { next = c; break; }
                 if (MODE == MODE_ONEHOT) {
                     sh.hist[nrej] = (u64)x;   // identical value written by every thread
                     ++nrej;
