@@ -159,7 +159,7 @@ __device__ __forceinline__ void argmax_combine(float& v, int& i, float v2, int i
 }
 
 template <int LDT, bool STOCH>
-__global__ void __launch_bounds__(kRowThreads) accept_rows_kernel(AcceptArgs a, int CL, int chunk, int rows_src) {
+__global__ void __launch_bounds__(kRowThreads) accept_rows_kernel(AcceptArgs a, int CL, int chunk, int rows_src, int lazy) {
     using LG = Logit<LDT>;
     using LT = typename LG::T;
     constexpr int VEC = LG::kVec;
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(kRowThreads) accept_rows_kernel(AcceptArgs a, 
     cluster.sync();   // partials consumed; s_part may be reused
 
     u64 S = 0;
-    const bool sums = STOCH && !a.lazy_sums;   // else the walk computes the sums of the rows it visits
+    const bool sums = STOCH && !lazy;   // else the walk computes the sums of the rows it visits
     if (sums && tot.fin) {
         const float m = tot.ymax;
         if (vec_ok) {
@@ -1045,17 +1045,16 @@ int pick_cluster(int V, int per_cta) {
 }
 
 template <int LDT>
-cudaError_t launch_typed(const AcceptArgs& args, cudaStream_t s) {
+cudaError_t launch_typed(const AcceptArgs& a, cudaStream_t s) {
     constexpr int VEC = Logit<LDT>::kVec;
-    const bool stoch = args.temperature > 0.f;
+    const bool stoch = a.temperature > 0.f;
     // Stochastic rows of a tree with many more nodes than a walk visits (T >= 16): the row kernel takes only
     // the max, min and first argmax of every row (every row must still be checked for non-finite logits), and
     // the walk computes the weight sums of the rows it visits.  Chains and small trees, whose walks visit most
     // rows, compute every row's sums in the row pass (measured on 32 chains of 6 nodes: 103 us with the sums in
     // the row pass against 110 us; on 8 trees of 60 nodes 89 against 76 us, on 128 trees of 64 nodes 1040
     // against 498 us).
-    AcceptArgs a = args;
-    a.lazy_sums = (stoch && a.T >= kLazySumsMinT) ? 1 : 0;
+    const int lazy = (stoch && a.T >= kLazySumsMinT) ? 1 : 0;
     const int mode = !stoch ? MODE_GREEDY : (a.draft ? MODE_PROB : MODE_ONEHOT);
     const int rows_src = a.B * a.T;
     const int rows = rows_src * (mode == MODE_PROB ? 2 : 1);
@@ -1064,7 +1063,7 @@ cudaError_t launch_typed(const AcceptArgs& args, cudaStream_t s) {
     // with at most about 9 CTAs per SM in all, which evens out the last wave (measured on 480 and 192 rows of
     // 128K-152K logits: 2 and 4).
     int CL;
-    if (stoch && !a.lazy_sums) {
+    if (stoch && !lazy) {
         CL = rows >= 8 * sm_count() ? 1 : pick_cluster(a.V, kRowThreads * VEC * 4);
     } else {
         const int cap = pick_cluster(a.V, kRowThreads * VEC * 4);
@@ -1080,7 +1079,7 @@ cudaError_t launch_typed(const AcceptArgs& args, cudaStream_t s) {
     const long long row_bytes = (long long)a.V * 2;
     while (CLs < kMaxCluster && row_bytes > (long long)CLs * 40 * 1024) CLs *= 2;
     int chunk_s = ((a.V + CLs - 1) / CLs + 7) / 8 * 8;
-    const bool staged = stoch && !a.lazy_sums && LDT == SV_BF16 && a.V % 8 == 0 && (long long)chunk_s * 2 <= kStoMaxSlice;
+    const bool staged = stoch && !lazy && LDT == SV_BF16 && a.V % 8 == 0 && (long long)chunk_s * 2 <= kStoMaxSlice;
     if (staged) {
         const size_t smem = (size_t)chunk_s * 2;
         // room for the slice, and the whole unified L1 as shared memory so several CTAs fit on an SM; function
@@ -1099,8 +1098,8 @@ cudaError_t launch_typed(const AcceptArgs& args, cudaStream_t s) {
         }
         if (a.argmax) e = launch_ex(accept_rows_staged_kernel<true>, dim3(CLs * rows), dim3(kStoThreads), smem, s, CLs, false, a, CLs, chunk_s, rows_src);
         else          e = launch_ex(accept_rows_staged_kernel<false>, dim3(CLs * rows), dim3(kStoThreads), smem, s, CLs, false, a, CLs, chunk_s, rows_src);
-    } else if (stoch) e = launch_ex(accept_rows_kernel<LDT, true>, dim3(CL * rows), dim3(kRowThreads), 0, s, CL, false, a, CL, chunk, rows_src);
-    else       e = launch_ex(accept_rows_kernel<LDT, false>, dim3(CL * rows), dim3(kRowThreads), 0, s, CL, false, a, CL, chunk, rows_src);
+    } else if (stoch) e = launch_ex(accept_rows_kernel<LDT, true>, dim3(CL * rows), dim3(kRowThreads), 0, s, CL, false, a, CL, chunk, rows_src, lazy);
+    else       e = launch_ex(accept_rows_kernel<LDT, false>, dim3(CL * rows), dim3(kRowThreads), 0, s, CL, false, a, CL, chunk, rows_src, 0);
     if (e != cudaSuccess) return e;
     // walk clusters: enough CTAs per request for the residual passes, but no more than the walk kernel keeps
     // resident at once over all requests (a second wave would repeat each request's serial chain of steps)
@@ -1113,10 +1112,10 @@ cudaError_t launch_typed(const AcceptArgs& args, cudaStream_t s) {
     switch (mode) {
     case MODE_GREEDY: return launch_ex(accept_walk_kernel<LDT, MODE_GREEDY, false>, gw, bw, 0, s, 1, true, a, 1);
     case MODE_PROB:
-        if (a.lazy_sums) return launch_ex(accept_walk_kernel<LDT, MODE_PROB, true>, gw, bw, 0, s, CLW, true, a, CLW);
+        if (lazy) return launch_ex(accept_walk_kernel<LDT, MODE_PROB, true>, gw, bw, 0, s, CLW, true, a, CLW);
         return launch_ex(accept_walk_kernel<LDT, MODE_PROB, false>, gw, bw, 0, s, CLW, true, a, CLW);
     default:
-        if (a.lazy_sums) return launch_ex(accept_walk_kernel<LDT, MODE_ONEHOT, true>, gw, bw, 0, s, CLW, true, a, CLW);
+        if (lazy) return launch_ex(accept_walk_kernel<LDT, MODE_ONEHOT, true>, gw, bw, 0, s, CLW, true, a, CLW);
         return launch_ex(accept_walk_kernel<LDT, MODE_ONEHOT, false>, gw, bw, 0, s, CLW, true, a, CLW);
     }
 }

@@ -322,6 +322,10 @@ size_t attn_bwd_workspace_size(int B, int T, int Hq) {
     return ((size_t)B * T * Hq * sizeof(float) + 255) / 256 * 256;
 }
 
+// the tensor-core kernels (attn_bwd_tc.cu)
+bool attn_bwd_tc_supported(const AttnBwdArgs& a);
+cudaError_t launch_attn_bwd_tc(const AttnBwdArgs& a, cudaStream_t s);
+
 cudaError_t launch_attn_bwd(const AttnBwdArgs& a, cudaStream_t s) {
     if (a.B == 0) return cudaSuccess;
     if (attn_bwd_tc_supported(a)) return launch_attn_bwd_tc(a, s);   // bf16, D = 128: tensor cores

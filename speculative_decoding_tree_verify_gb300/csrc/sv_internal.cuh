@@ -112,9 +112,6 @@ struct AcceptArgs {
     int32_t* argmax;
     int32_t* status;
     void* ws;
-    // stochastic modes: the row kernel leaves the weight sums to the walk, which computes them for the rows it
-    // visits only
-    int lazy_sums = 0;
 };
 
 size_t accept_workspace_size(int B, int T, int V);
@@ -159,8 +156,6 @@ struct AttnBwdArgs {
 
 size_t attn_bwd_workspace_size(int B, int T, int Hq);
 cudaError_t launch_attn_bwd(const AttnBwdArgs& a, cudaStream_t s);
-bool attn_bwd_tc_supported(const AttnBwdArgs& a);
-cudaError_t launch_attn_bwd_tc(const AttnBwdArgs& a, cudaStream_t s);
 
 struct CompactArgs {
     int B, T, Hkv, D, kv_cap;
